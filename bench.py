@@ -1,0 +1,427 @@
+#!/usr/bin/env python
+"""Throughput of the Compass-style decoder path on GB300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one whole pass of the path over one batch of synthetic input: the layer stack
+and the tied head. `value` is prefill tokens/s on the two-layer pair workload (sliding
+layer with MRoPE + full NoPE layer, bf16, T = 2048 with one 16x16 image at token 300 and
+a deepstack add after layer 0, head on the last token over a 256000 vocabulary); the
+`decode` object is the batched decode step (64 sequences x 4096 cached tokens, paged KV,
+head on all 64 rows). Inputs are resident in HBM when the timed region starts; every
+step reads 1.3 GB of weights (more than the 129 MB L2), so no flush is needed. `e2e`
+repeats the prefill measurement with host buffers: the step's inputs are copied from
+pinned host memory and its logits copied back inside the timed region.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path
+does not shard within a step); value = tokens of all ranks / max time over ranks.
+`--impl reference` times the CPU oracle (fp64 NumPy) as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s and decode tokens/s (1 GB300) + % of bf16 tensor / HBM roofline"
+PREFILL_DESC = ("two-layer pair (sliding+interleaved MRoPE, full NoPE), bf16, batch 1, "
+                "seq 2048, hidden 2048, 16/4 heads, head_dim 128, SwiGLU 8192, window 512, "
+                "one 16x16 image at token 300, deepstack [256,2048] after layer 0, tied head "
+                "on the last token, vocab 256000")
+DECODE_DESC = ("decode step on the two-layer pair: 64 sequences x 4096 cached bf16 tokens in "
+               "16-token pages (permuted page table), window 4096, head on all 64 rows")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-tokens", type=int, default=0,
+                   help="oracle sample: first N tokens of the prefill workload (0: all)")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------------------ dist
+class Dist:
+    def __init__(self, n):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if _cuda() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x):
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if _cuda() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda():
+    import torch
+    return torch.cuda.is_available()
+
+
+# ------------------------------------------------------------------------------ clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        busy = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------ timing
+def time_steps(fn, steps, warmup, dist, stream):
+    """W untimed steps, then exactly K steps bracketed by barrier + synchronize; CUDA
+    events on the launching stream; returns the max over ranks in ms."""
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        fn(warmup + k)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    return dist.max(t0.elapsed_time(t1))
+
+
+def kernel_profile(gw, fn, steps, base):
+    """Per kernel class: launches and mean device time per launch, from the library's
+    CUDA-event records over `steps` further steps."""
+    import torch
+    import cohere_compass_decoder_gb300._lib as L
+    L.cc_profile_read(gw.stack.plan)
+    L.cc_profile_enable(gw.stack.plan, True)
+    for k in range(steps):
+        fn(base + k)
+    torch.cuda.synchronize()
+    prof = L.cc_profile_read(gw.stack.plan)
+    L.cc_profile_enable(gw.stack.plan, False)
+    total = sum(ms for _, ms in prof.values()) or 1.0
+    out = {}
+    for name, (n, ms) in prof.items():
+        if n:
+            out[name] = {"launches_per_step": n / steps, "avg_us": 1000.0 * ms / n,
+                         "share": ms / total}
+    return out
+
+
+# ------------------------------------------------------------------------------ legs
+def prefill_leg(args, dist, pk):
+    import numpy as np
+    import torch
+    from synth import Inputs
+    from synth.configs import cfg2
+    from cohere_compass_decoder_gb300.workload import GpuWorkload
+
+    inp = Inputs(cfg2())
+    gw = GpuWorkload(inp)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    n_prof = max(3, min(K, 10))
+    pool = [gw.fresh_hidden() for _ in range(K + W + n_prof)]
+    logits = torch.empty(len(inp.head_rows), inp.shape.vocab_size, device="cuda")
+
+    def step(i):
+        gw.step(pool[i], logits)
+
+    ms = time_steps(step, K, W, dist, stream)
+    gw.sync()
+    kern = kernel_profile(gw, step, n_prof, K + W)
+    T = inp.wl.total_tokens
+    s = inp.shape
+    N1 = (s.num_attention_heads + 2 * s.num_key_value_heads) * s.head_dim + 2 * s.intermediate_size
+    g1 = kern.get("gemm_qkv_mlp", {})
+    flops = 2.0 * T * N1 * s.hidden_size
+    ach = flops / (g1["avg_us"] * 1e-6) / 1e12 if g1 else None
+    roof = {"kernel": "gemm_qkv_mlp", "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
+            "unit": "TFLOP/s", "frac": (ach / pk["bf16"]) if ach else None, "traffic": None,
+            "peak_source": f"{pk['src']} bf16 burst (of {pk['src']})",
+            "algorithmic_per_launch": f"2*T*N1*H = {flops:.4g} FLOP"}
+    # other classes against their own roofs
+    g2 = kern.get("gemm_out_resid")
+    if g2:
+        K2 = s.num_attention_heads * s.head_dim + s.intermediate_size
+        f2 = 2.0 * T * s.hidden_size * K2
+        g2["tflops"] = f2 / (g2["avg_us"] * 1e-6) / 1e12
+        g2["frac_of_bf16_peak"] = g2["tflops"] / pk["bf16"]
+    at = kern.get("attn_prefill")
+    if at:
+        fa = attn_flops(inp) / at["launches_per_step"]
+        at["tflops"] = fa / (at["avg_us"] * 1e-6) / 1e12
+        at["frac_of_bf16_peak"] = at["tflops"] / pk["bf16"]
+    value = T * K * dist.world / (ms / 1e3)
+    launches = sum(v["launches_per_step"] for v in kern.values())
+    extra = kern.get("row_maps", {}).get("launches_per_step", 0) and 1  # ds map: fill + scatter
+    res = dict(ms=ms, value=value, kernels=kern, roofline=roof,
+               launches=int(round((launches + extra) * K)))
+    # e2e through host buffers
+    if not args.no_e2e:
+        res["e2e"] = prefill_e2e(gw, inp, K, W, dist, stream)
+    gw.close()
+    return res
+
+
+def attn_flops(inp):
+    """4 * d * n_q * (visible keys summed over queries) over all layers of the workload."""
+    s = inp.shape
+    total = 0
+    for lt in s.layer_types:
+        W = s.sliding_window if lt == "sliding_attention" else None
+        for L in inp.wl.seq_lens:
+            i = __import__("numpy").arange(L)
+            vis = i + 1 if W is None else __import__("numpy").minimum(i + 1, W)
+            total += int(vis.sum())
+    return 4.0 * s.head_dim * s.num_attention_heads * total
+
+
+def prefill_e2e(gw, inp, K, W, dist, stream):
+    import torch
+    host_h = torch.from_numpy(inp.hidden).pin_memory()
+    host_pos = gw.pos.cpu().pin_memory()
+    host_cu = gw.cu.cpu().pin_memory()
+    host_rows = gw.ds_rows.cpu().pin_memory()
+    host_ds = [f.cpu().pin_memory() for f in gw.ds_feats]
+    n_out = len(inp.head_rows) * inp.shape.vocab_size
+    host_out = torch.empty(n_out, dtype=torch.float32).pin_memory()
+    dev_h = torch.empty_like(gw.hidden0)
+    logits = torch.empty(len(inp.head_rows), inp.shape.vocab_size, device="cuda")
+    bi = (host_h.numel() * 4 + host_pos.numel() * 4 + host_cu.numel() * 4 + host_rows.numel() * 4
+          + sum(f.numel() * f.element_size() for f in host_ds))
+    bo = n_out * 4
+
+    def step(i):
+        dev_h.copy_(host_h, non_blocking=True)
+        gw.pos.copy_(host_pos, non_blocking=True)
+        gw.cu.copy_(host_cu, non_blocking=True)
+        gw.ds_rows.copy_(host_rows, non_blocking=True)
+        for d, h in zip(gw.ds_feats, host_ds):
+            d.copy_(h, non_blocking=True)
+        gw.step(dev_h, logits)
+        host_out.copy_(logits.view(-1), non_blocking=True)
+
+    ms = time_steps(step, K, W, dist, stream)
+    T = inp.wl.total_tokens
+    return {"value": T * K * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / K,
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+
+
+def decode_leg(args, dist, pk):
+    import torch
+    from synth import Inputs
+    from synth.configs import cfg4
+    from cohere_compass_decoder_gb300.workload import GpuWorkload
+
+    inp = Inputs(cfg4())
+    gw = GpuWorkload(inp)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    n_prof = max(3, min(K, 10))
+    pool = [gw.fresh_hidden() for _ in range(K + W + n_prof)]
+    logits = torch.empty(len(inp.head_rows), inp.shape.vocab_size, device="cuda")
+
+    def step(i):
+        gw.step(pool[i], logits)
+
+    ms = time_steps(step, K, W, dist, stream)
+    gw.sync()
+    kern = kernel_profile(gw, step, n_prof, K + W)
+    s = inp.shape
+    B = inp.wl.decode_batch
+    n = inp.wl.cache_len + 1
+    kv_bytes = 0
+    for lt in s.layer_types:
+        keys = min(n, s.sliding_window) if lt == "sliding_attention" else n
+        kv_bytes += B * keys * s.num_key_value_heads * s.head_dim * 2 * 2
+    ad = kern.get("attn_decode")
+    per_launch = kv_bytes / len(s.layer_types)
+    ach = per_launch / (ad["avg_us"] * 1e-6) / 1e9 if ad else None
+    roof = {"kernel": "attn_decode", "bound": "hbm", "achieved": ach, "peak": pk["hbm"],
+            "unit": "GB/s", "frac": (ach / pk["hbm"]) if ach else None, "traffic": None,
+            "peak_source": f"HBM copy (of {pk['src']})",
+            "algorithmic_per_launch": f"K+V of the visible keys, {per_launch:.4g} B"}
+    gh = kern.get("gemm_head")
+    if gh:
+        hb = s.vocab_size * s.hidden_size * 2 + B * s.vocab_size * 4
+        gh["gbs"] = hb / (gh["avg_us"] * 1e-6) / 1e9
+        gh["frac_of_hbm"] = gh["gbs"] / pk["hbm"]
+    value = B * K * dist.world / (ms / 1e3)
+    launches = sum(v["launches_per_step"] for v in kern.values())
+    launches += kern.get("attn_decode", {}).get("launches_per_step", 0)  # + split combine
+    gw.close()
+    return dict(ms=ms, value=value, kernels=kern, roofline=roof, launches=int(round(launches * K)))
+
+
+def cpu_baseline(args, tokens=0):
+    """The oracle (fp64 NumPy, as it stands) on the prefill workload or its first tokens."""
+    import numpy as np
+    from synth import Inputs
+    from synth.configs import cfg2, Workload
+    from oracle import runs
+
+    wl = cfg2()
+    if tokens and tokens < wl.total_tokens:
+        imgs = [i for i in wl.images if i.start + i.n_tokens <= tokens]
+        wl = Workload(wl.name + f"_first{tokens}", wl.shape, "prefill", [tokens], images=imgs,
+                      n_deepstack=wl.n_deepstack if imgs else 0, head_rows="last", seed=wl.seed)
+    inp = Inputs(wl)
+    for i in range(wl.shape.num_layers):
+        inp.layer(i)
+    _ = inp.embed
+    t0 = time.perf_counter()
+    runs.run_prefill(inp)
+    dt = time.perf_counter() - t0
+    return {"value": wl.total_tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"one prefill + head of {wl.total_tokens} tokens of the prefill workload "
+                      f"(fp64 NumPy, BLAS on all host cores)"}
+
+
+def run_reference(args):
+    dist_rank = int(os.environ.get("RANK", "0"))
+    if dist_rank != 0:
+        return 0
+    tokens = args.cpu_tokens
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(args, tokens)
+        if i >= args.warmup:
+            vals.append(r)
+    secs = sum(r["seconds"] for r in vals)
+    T = vals[0]["value"] * vals[0]["seconds"]
+    value = T * len(vals) / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * secs / len(vals), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": PREFILL_DESC, "global_batch": 1, "seq_len": 2048,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": vals[0]["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    dist = Dist(args.gpus)
+    torch.cuda.set_device(dist.local)
+    import cohere_compass_decoder_gb300 as pkg
+    if not os.path.exists(pkg._lib.LIB_PATH):
+        from cohere_compass_decoder_gb300.build import build
+        build()
+    pk = peaks()
+    clocks = Clocks(dist.local) if dist.rank == 0 else None
+    t_start = time.time()
+    pre = prefill_leg(args, dist, pk)
+    dec = None if args.no_decode else decode_leg(args, dist, pk)
+    # keep the clock sampler running for at least ~1 s of GPU work
+    if clocks and time.time() - t_start < 1.5:
+        time.sleep(0.1)
+    clk = clocks.stop() if clocks else None
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, args.cpu_tokens)
+        cpu.pop("seconds", None)
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"] / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": PREFILL_DESC, "global_batch": 1, "seq_len": 2048,
+                       "parallelism": "replicas" if dist.world > 1 else "single",
+                       "l2": "inputs larger than L2 (1.3 GB of weights per step)"},
+            "roofline": pre["roofline"], "cpu_baseline": cpu,
+            "e2e": pre.get("e2e"), "gpu_launches": pre["launches"], "clocks": clk,
+            "kernels": pre["kernels"],
+        }
+        if dec:
+            line["decode"] = {"workload": DECODE_DESC, "value": dec["value"], "unit": "tokens/s",
+                              "ms_per_step": dec["ms"] / args.steps, "roofline": dec["roofline"],
+                              "gpu_launches": dec["launches"], "kernels": dec["kernels"]}
+        print(json.dumps(line))
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

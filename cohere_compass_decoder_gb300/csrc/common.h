@@ -1,0 +1,48 @@
+// Shared constants and host helpers of the cc library (device-independent parts).
+#pragma once
+
+#include <cstdint>
+#include <cstdio>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/cc.h"
+
+namespace cc {
+
+// Device error codes written to the sticky error flag (same values as cc_status).
+enum : int { CC_DEV_TIMEOUT = CC_ERR_TIMEOUT, CC_DEV_CHECK = CC_ERR_DEVICE_CHECK };
+
+// A bounded inter-warp wait gives up after this long (no launch here runs for seconds).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+constexpr int kNumSMsFallback = 152;
+
+// ------------------------------------------------------------------ host helpers
+#define CC_CHECK_CUDA(expr)                                                        \
+  do {                                                                             \
+    cudaError_t e_ = (expr);                                                       \
+    if (e_ != cudaSuccess) {                                                       \
+      cc::last_cuda_error() = e_;                                                  \
+      return CC_ERR_CUDA;                                                          \
+    }                                                                              \
+  } while (0)
+
+#define CC_CHECK_STATUS(expr)                                                      \
+  do {                                                                             \
+    cc_status s_ = (expr);                                                         \
+    if (s_ != CC_OK) return s_;                                                    \
+  } while (0)
+
+cudaError_t& last_cuda_error();
+
+// Number of SMs of the current device (cached per process).
+int num_sms();
+
+// 2-D bf16 tensor map for TMA: a [rows, cols] row-major matrix with leading dimension
+// `ld` elements, boxes of box_cols x box_rows, 128-byte swizzle when box_cols*2 == 128.
+// Zero fill out of bounds. Returns false on failure (bad alignment or driver error).
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
+}  // namespace cc

@@ -1,0 +1,117 @@
+// Internal launchers of the cc kernels (not part of the C-ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "common.h"
+
+namespace cc {
+
+// ---------------------------------------------------------------- GEMM (tcgen05)
+enum EpiMode : int {
+  EPI_F32 = 0,      // c = alpha * acc (+ c)
+  EPI_RESID = 1,    // h += acc (+ deepstack row)
+  EPI_QKV_MLP = 2,  // column-typed: q / k / v heads (+ rotation, + paged K/V), SwiGLU
+};
+
+struct EpiParams {
+  // EPI_F32 and EPI_RESID: fp32 output / residual, leading dimension ldc
+  float* c = nullptr;
+  int ldc = 0;
+  float alpha = 1.f;
+  int accumulate = 0;
+  // EPI_RESID: deepstack add, ds_map[row] = index into ds (or -1)
+  const int32_t* ds_map = nullptr;
+  const __nv_bfloat16* ds = nullptr;
+  // EPI_QKV_MLP: columns [0, q_cols) q heads, then kv_cols of k, kv_cols of v, then the
+  // SwiGLU region in 128-column blocks (64 gate columns, then the 64 matching up columns)
+  int q_cols = 0, kv_cols = 0, n_kv = 0;
+  const float2* rope = nullptr;          // [M, 64] (cos, sin), null: no rotation
+  __nv_bfloat16* q_out = nullptr;        // [M, ld_q]
+  int ld_q = 0;
+  __nv_bfloat16* k_out = nullptr;        // [M, ld_kv] contiguous copy (nullable)
+  __nv_bfloat16* v_out = nullptr;
+  int ld_kv = 0;
+  __nv_bfloat16* k_pool = nullptr;       // paged copy (nullable)
+  __nv_bfloat16* v_pool = nullptr;
+  const int32_t* kv_slot = nullptr;      // [M] flat slot page*page_size + offset, <0: skip
+  int page_size = 16;
+  __nv_bfloat16* act_out = nullptr;      // [M, ld_act]
+  int ld_act = 0;
+};
+
+// C[M,N] (epilogue) = A[M,K] @ B[N,K]^T with A, B given by TMA maps (bf16, box 64 x 128
+// for A and 64 x BN for B, 128-byte swizzle). bn is 128 or 256; splits divides the
+// K loop (splits > 1 needs an additive epilogue: EPI_RESID or EPI_F32 with accumulate).
+cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int bn,
+                      int splits, int epi, const EpiParams& ep, int* err, cudaStream_t s);
+
+// Picks bn / splits for a problem (used by every caller of launch_gemm).
+void gemm_choose(int M, int N, int K, int epi, int* bn, int* splits);
+
+// ---------------------------------------------------------------- attention
+struct AttnTile {
+  int32_t seq_start;  // first token of the sequence in the packed batch
+  int32_t seq_len;
+  int32_t q0;         // first query (relative to the sequence) of this 128-row tile
+  int32_t pad;
+};
+
+// Builds the list of 128-query tiles of all sequences, heaviest first.
+cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int window, AttnTile* tiles,
+                            int32_t* n_tiles, cudaStream_t s);
+int attn_max_tiles(int tokens, int n_seqs);
+
+cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              __nv_bfloat16* out, int ld_out, const AttnTile* tiles,
+                              const int32_t* n_tiles, int max_tiles, int n_q, int n_kv,
+                              int window, int* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- decode attention
+struct DecodeScratch {
+  float* part_o = nullptr;   // [batch, n_q, splits, 128]
+  float* part_ml = nullptr;  // [batch, n_q, splits, 2]
+};
+int decode_splits(int max_pages);
+size_t decode_scratch_floats(int batch, int n_q, int max_pages);
+cc_status launch_attn_decode(const __nv_bfloat16* q, int ld_q, const __nv_bfloat16* k_pool,
+                             const __nv_bfloat16* v_pool, int n_pages, const int32_t* page_table,
+                             int max_pages, const int32_t* n_keys, int batch, int n_q, int n_kv,
+                             int page_size, int window, DecodeScratch scr, __nv_bfloat16* out,
+                             int ld_out, int* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- small kernels
+cc_status launch_layernorm_bf16(const float* x, const __nv_bfloat16* gamma, __nv_bfloat16* out,
+                                int rows, int H, float eps, const int32_t* row_idx,
+                                cudaStream_t s);
+cc_status launch_layernorm_f32(const float* x, const float* gamma, float* out, int rows, int H,
+                               float eps, const int32_t* row_idx, cudaStream_t s);
+cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double theta,
+                             const int32_t section[3], float2* table, cudaStream_t s);
+cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, int* err,
+                        cudaStream_t s);
+// kv_slot for prefill tokens: page_table[seq, t / ps] * ps + t % ps
+cc_status launch_kv_slots_prefill(const int32_t* cu_seqlens, int n_seqs, int T,
+                                  const int32_t* page_table, int max_pages, int page_size,
+                                  int n_pages, int32_t* slots, int* err, cudaStream_t s);
+// kv_slot of decode rows: the new token of sequence b goes to slot seq_lens[b]
+cc_status launch_kv_slots_decode(const int32_t* seq_lens, int batch, const int32_t* page_table,
+                                 int max_pages, int page_size, int n_pages, int32_t* slots,
+                                 int32_t* n_keys, int* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- fp32 (CUDA-core) path
+cc_status launch_gemm_f32(const float* a, int lda, const float* b, int ldb, float* c, int ldc,
+                          int M, int N, int K, float alpha, int accumulate, cudaStream_t s);
+cc_status launch_qkv_mlp_f32(const float* y, int ldy, int M, int q_cols, int kv_cols,
+                             int head_dim, int inter, const float2* rope, float* q, float* k,
+                             float* v, float* act, int ld_act, cudaStream_t s);
+cc_status launch_attn_f32(const float* q, const float* k, const float* v, float* out,
+                          int ld_out, const int32_t* cu_seqlens, int n_seqs, int T, int n_q,
+                          int n_kv, int head_dim, int window, cudaStream_t s);
+cc_status launch_ds_add_f32(float* h, int H, const int32_t* rows, int n_rows, const float* ds,
+                            cudaStream_t s);
+
+}  // namespace cc

@@ -1,0 +1,226 @@
+// Memory-bound helpers of the path: LayerNorm, the MRoPE cos/sin table, row maps.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace cc {
+
+namespace {
+
+// ---------------------------------------------------------------------- LayerNorm
+// mlxcel issue "Cohere Compass / North-Micro-Vision", "Text decoder forward": LayerNorm
+// with weight only (no bias), statistics in f32; biased variance, eps inside the root.
+// One warp per row; two passes over the row (mean, then centred second moment) kept in
+// registers (H / 128 float4 per lane, H <= 128 * kMaxV4).
+constexpr int kMaxV4 = 32;  // H <= 4096 in the register-resident variant
+
+template <int NV4, typename OutT>
+__global__ void __launch_bounds__(256)
+    k_layernorm(const float* __restrict__ x, const void* __restrict__ gamma,
+                OutT* __restrict__ out, int rows, int H, float eps,
+                const int32_t* __restrict__ row_idx, int gamma_bf16) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int src = row_idx ? row_idx[row] : row;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * H);
+  float4 v[NV4];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    v[i] = xr[lane + 32 * i];
+    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mean = s / H;
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+    q += (a * a + b * b) + (c * c + d * d);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  const float rstd = rsqrtf(q / H + eps);
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    const int c0 = 4 * (lane + 32 * i);
+    float g0, g1, g2, g3;
+    if (gamma_bf16) {
+      const __nv_bfloat162* gp = reinterpret_cast<const __nv_bfloat162*>(
+          reinterpret_cast<const __nv_bfloat16*>(gamma) + c0);
+      const float2 a = __bfloat1622float2(gp[0]), b = __bfloat1622float2(gp[1]);
+      g0 = a.x; g1 = a.y; g2 = b.x; g3 = b.y;
+    } else {
+      const float4 gg = reinterpret_cast<const float4*>(gamma)[c0 / 4];
+      g0 = gg.x; g1 = gg.y; g2 = gg.z; g3 = gg.w;
+    }
+    const float y0 = (v[i].x - mean) * rstd * g0, y1 = (v[i].y - mean) * rstd * g1;
+    const float y2 = (v[i].z - mean) * rstd * g2, y3 = (v[i].w - mean) * rstd * g3;
+    if constexpr (sizeof(OutT) == 2) {
+      uint2 pk;
+      pk.x = pack_bf16x2(y0, y1);
+      pk.y = pack_bf16x2(y2, y3);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)row * H + c0) = pk;
+    } else {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)row * H + c0) =
+          make_float4(y0, y1, y2, y3);
+    }
+  }
+}
+
+template <typename OutT>
+cc_status launch_ln(const float* x, const void* gamma, OutT* out, int rows, int H, float eps,
+                    const int32_t* row_idx, int gamma_bf16, cudaStream_t s) {
+  if (rows <= 0) return CC_OK;
+  if (H % 128 != 0 || H > 128 * kMaxV4) return CC_ERR_UNSUPPORTED;
+  const int nv4 = H / 128;
+  const dim3 grid((rows + 7) / 8);
+#define CC_LN_CASE(N) \
+  case N: k_layernorm<N, OutT><<<grid, 256, 0, s>>>(x, gamma, out, rows, H, eps, row_idx, gamma_bf16); break;
+  switch (nv4) {
+    CC_LN_CASE(1) CC_LN_CASE(2) CC_LN_CASE(3) CC_LN_CASE(4) CC_LN_CASE(6) CC_LN_CASE(8)
+    CC_LN_CASE(12) CC_LN_CASE(16) CC_LN_CASE(24) CC_LN_CASE(32)
+    default: return CC_ERR_UNSUPPORTED;
+  }
+#undef CC_LN_CASE
+  CC_CHECK_CUDA(cudaGetLastError());
+  return CC_OK;
+}
+
+// ---------------------------------------------------------------------- MRoPE table
+// mlxcel issue "Text decoder forward", interleaved MRoPE: frequency j (< d/2) reads the h
+// axis when j % 3 == 1 and j < 3 s_h, the w axis when j % 3 == 2 and j < 3 s_w, else t;
+// angle = pos[axis] * theta^(-2j/d). The angle (up to ~1e5 rad) is formed and reduced
+// modulo 2*pi in double precision; sincosf then sees |r| <= pi.
+__global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, double theta,
+                              int sec_h, int sec_w, float2* __restrict__ table) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= T * half) return;
+  const int t = idx / half, j = idx - t * half;
+  int axis = 0;
+  if (j % 3 == 1 && j < 3 * sec_h) axis = 1;
+  else if (j % 3 == 2 && j < 3 * sec_w) axis = 2;
+  const double inv_freq = pow(theta, -2.0 * j / (2.0 * half));
+  const double ang = static_cast<double>(pos[axis * T + t]) * inv_freq;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double r = ang - two_pi * rint(ang / two_pi);
+  float sn, cs;
+  sincosf(static_cast<float>(r), &sn, &cs);
+  table[idx] = make_float2(cs, sn);
+}
+
+// ---------------------------------------------------------------------- row maps
+__global__ void k_fill_i32(int32_t* p, int n, int32_t v) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+__global__ void k_ds_map(const int32_t* __restrict__ rows, int n_rows, int T,
+                         int32_t* __restrict__ map, int* err) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows) return;
+  const int t = rows[r];
+  if (t < 0 || t >= T) {
+    set_error(err, CC_DEV_CHECK);
+    return;
+  }
+  map[t] = r;
+}
+
+__global__ void k_kv_slots_prefill(const int32_t* __restrict__ cu, int n_seqs, int T,
+                                   const int32_t* __restrict__ pt, int max_pages, int ps,
+                                   int n_pages, int32_t* __restrict__ slots, int* err) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  int lo = 0, hi = n_seqs;  // sequence s with cu[s] <= t < cu[s+1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int pos = t - cu[lo];
+  const int pi = pos / ps;
+  int slot = -1;
+  if (pi < max_pages) {
+    const int page = pt[(size_t)lo * max_pages + pi];
+    if (page >= 0 && page < n_pages) slot = page * ps + (pos - pi * ps);
+  }
+  if (slot < 0) set_error(err, CC_DEV_CHECK);
+  slots[t] = slot;
+}
+
+__global__ void k_kv_slots_decode(const int32_t* __restrict__ seq_lens, int batch,
+                                  const int32_t* __restrict__ pt, int max_pages, int ps,
+                                  int n_pages, int32_t* __restrict__ slots,
+                                  int32_t* __restrict__ n_keys, int* err) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int pos = seq_lens[b];
+  const int pi = pos / ps;
+  int slot = -1;
+  if (pos >= 0 && pi < max_pages) {
+    const int page = pt[(size_t)b * max_pages + pi];
+    if (page >= 0 && page < n_pages) slot = page * ps + (pos - pi * ps);
+  }
+  if (slot < 0) set_error(err, CC_DEV_CHECK);
+  slots[b] = slot;
+  n_keys[b] = slot < 0 ? 0 : pos + 1;
+}
+
+}  // namespace
+
+cc_status launch_layernorm_bf16(const float* x, const __nv_bfloat16* gamma, __nv_bfloat16* out,
+                                int rows, int H, float eps, const int32_t* row_idx,
+                                cudaStream_t s) {
+  return launch_ln<__nv_bfloat16>(x, gamma, out, rows, H, eps, row_idx, 1, s);
+}
+
+cc_status launch_layernorm_f32(const float* x, const float* gamma, float* out, int rows, int H,
+                               float eps, const int32_t* row_idx, cudaStream_t s) {
+  return launch_ln<float>(x, gamma, out, rows, H, eps, row_idx, 0, s);
+}
+
+cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double theta,
+                             const int32_t section[3], float2* table, cudaStream_t s) {
+  if (T <= 0) return CC_OK;
+  const int half = head_dim / 2;
+  const int n = T * half;
+  k_mrope_table<<<(n + 255) / 256, 256, 0, s>>>(pos, T, half, theta, section[1], section[2],
+                                                table);
+  CC_CHECK_CUDA(cudaGetLastError());
+  return CC_OK;
+}
+
+cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, int* err,
+                        cudaStream_t s) {
+  if (T <= 0) return CC_OK;
+  k_fill_i32<<<(T + 255) / 256, 256, 0, s>>>(map, T, -1);
+  CC_CHECK_CUDA(cudaGetLastError());
+  if (n_rows > 0) {
+    k_ds_map<<<(n_rows + 255) / 256, 256, 0, s>>>(rows, n_rows, T, map, err);
+    CC_CHECK_CUDA(cudaGetLastError());
+  }
+  return CC_OK;
+}
+
+cc_status launch_kv_slots_prefill(const int32_t* cu_seqlens, int n_seqs, int T,
+                                  const int32_t* page_table, int max_pages, int page_size,
+                                  int n_pages, int32_t* slots, int* err, cudaStream_t s) {
+  if (T <= 0) return CC_OK;
+  k_kv_slots_prefill<<<(T + 255) / 256, 256, 0, s>>>(cu_seqlens, n_seqs, T, page_table, max_pages,
+                                                     page_size, n_pages, slots, err);
+  CC_CHECK_CUDA(cudaGetLastError());
+  return CC_OK;
+}
+
+cc_status launch_kv_slots_decode(const int32_t* seq_lens, int batch, const int32_t* page_table,
+                                 int max_pages, int page_size, int n_pages, int32_t* slots,
+                                 int32_t* n_keys, int* err, cudaStream_t s) {
+  if (batch <= 0) return CC_OK;
+  k_kv_slots_decode<<<(batch + 127) / 128, 128, 0, s>>>(seq_lens, batch, page_table, max_pages,
+                                                        page_size, n_pages, slots, n_keys, err);
+  CC_CHECK_CUDA(cudaGetLastError());
+  return CC_OK;
+}
+
+}  // namespace cc

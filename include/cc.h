@@ -1,0 +1,278 @@
+/*
+ * cc.h -- C-ABI of the GB300 (sm_103a) Compass-style parallel decoder stack.
+ *
+ * The library computes the forward pass of the Cohere2/Compass parallel decoder layer
+ * stack over a merged image+text sequence, as defined by the mlxcel issue
+ * "feat(vlm): add Cohere Compass / North-Micro-Vision (cohere_compass) VLM", section
+ * "Text decoder forward":
+ *
+ *   for each layer i:  a = LayerNorm_i(h)                      (weight only, f32 statistics)
+ *                      h = h + Attn_i(a) + SwiGLU_i(a)         (parallel block, no post-norm)
+ *                      if i < n_deepstack: h[image rows] += deepstack[i]
+ *   logits = logit_scale * (LayerNorm_f(h) @ embed^T)          (tied head)
+ *
+ * Sliding layers rotate q and k with the interleaved 3-axis MRoPE (split rotate-half)
+ * and attend causally over the last `sliding_window` keys; full layers use no position
+ * encoding and plain causal attention. Attention is grouped-query (query head h reads
+ * KV head h / (n_q / n_kv)) with scale head_dim^-0.5.
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are DEVICE pointers owned by the caller unless the comment says
+ *    "host". Matrices are row-major and dense (leading dimension = row length) unless a
+ *    leading dimension is passed.
+ *  - `stream` is a cudaStream_t passed as void*; every call is stream-ordered and
+ *    asynchronous (no host synchronisation), except the host helpers.
+ *  - Errors found on the host return a status and launch nothing. Errors found on the
+ *    device (a bounded wait that ran out, a bad index) set a sticky device flag that
+ *    cc_sync / cc_op_sync returns; the results of the affected calls are undefined.
+ *  - No call aborts the process or throws across the ABI.
+ *  - bf16 tensors hold raw bfloat16 bit patterns; f32 tensors hold IEEE floats.
+ */
+#ifndef CC_H_
+#define CC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CC_OK = 0,
+  CC_ERR_INVALID_ARG = 1,   /* a host-detectable argument error                       */
+  CC_ERR_UNSUPPORTED = 2,   /* a valid configuration this build does not implement    */
+  CC_ERR_OOM = 3,           /* device allocation failed                               */
+  CC_ERR_CUDA = 4,          /* a CUDA runtime call failed (launch, copy, attribute)    */
+  CC_ERR_TIMEOUT = 5,       /* device: a bounded inter-warp wait gave up              */
+  CC_ERR_DEVICE_CHECK = 6   /* device: an index check failed (page id, row map)       */
+} cc_status;
+
+typedef enum { CC_SLIDING = 0, CC_FULL = 1 } cc_layer_type;
+typedef enum { CC_F32 = 0, CC_BF16 = 1 } cc_dtype;
+
+/* Model hyper-parameters: the text_config keys of the Compass checkpoint (mlxcel issue,
+ * "Config (config.json)" and "Text decoder forward"). `layer_types` points to
+ * num_layers entries of cc_layer_type and is copied by cc_layer_plan_create.
+ * Requirements (else CC_ERR_INVALID_ARG): mrope_section sums to head_dim/2;
+ * n_q_heads % n_kv_heads == 0; sliding_window > 0; all sizes > 0.
+ * bf16 plans also need (else CC_ERR_UNSUPPORTED): head_dim == 128; hidden_size and
+ * intermediate_size multiples of 128; (n_q + 2*n_kv)*head_dim a multiple of 256;
+ * vocab_size a multiple of 128. f32 plans need head_dim <= 128 and even. */
+typedef struct {
+  int32_t num_layers;
+  int32_t hidden_size;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t intermediate_size;
+  int32_t vocab_size;
+  int32_t sliding_window;
+  int32_t mrope_section[3];   /* frequencies on the t, h, w axes                        */
+  int32_t kv_page_size;       /* tokens per KV page (paged cache), e.g. 16              */
+  int32_t max_tokens;         /* largest token count of one call; sizes the workspace   */
+  int32_t dtype;              /* cc_dtype of weights and stored activations             */
+  const int32_t* layer_types; /* host [num_layers]                                     */
+  double rope_theta;
+  float layer_norm_eps;
+  float logit_scale;
+} cc_model_config;
+
+/* One layer's weights, packed by cc_pack_layer_weights:
+ *  ln_w [H]                    LayerNorm gain
+ *  w1   [N1, H], N1 = (n_q + 2 n_kv) d + 2 I: rows q | k | v | then the SwiGLU gate and
+ *       up rows interleaved in blocks of 128 (gate 0..127, up 0..127, gate 128..255, ...)
+ *  w2   [H, K2], K2 = n_q d + I: columns o_proj | down_proj
+ * The plan borrows these pointers; they must outlive it. */
+typedef struct {
+  const void* ln_w;
+  const void* w1;
+  const void* w2;
+} cc_layer_weights;
+
+/* Paged KV cache of every layer: k[i], v[i] point to [n_pages, n_kv, page_size, head_dim]
+ * bf16 pools (caller-owned, host array of device pointers, num_layers entries each).
+ * Keys are stored after rotation (sliding layers) or as projected (full layers).
+ * Token t of sequence b lives in page page_table[b * max_pages + t / page_size], slot
+ * t % page_size. */
+typedef struct {
+  void* const* k;
+  void* const* v;
+  int32_t n_pages;
+} cc_kv_pool;
+
+/* One image inside a packed batch: merged grid (t, h, w) occupying t*h*w consecutive
+ * tokens of sequence `seq`, starting at token offset `start` of that sequence. */
+typedef struct {
+  int32_t seq;
+  int32_t start;
+  int32_t grid_t;
+  int32_t grid_h;
+  int32_t grid_w;
+} cc_image_span;
+
+typedef struct cc_layer_plan cc_layer_plan;
+
+/* ---------------------------------------------------------------------------------- */
+const char* cc_status_string(cc_status s);
+
+/* Host helper (no device work). Position ids of packed sequences, mlxcel issue
+ * "Text decoder forward", paragraph "Position ids (get_rope_index)": text tokens take
+ * max(previous positions)+1 on all three axes (0 for a sequence's first token); the
+ * t*h*w tokens of an image take offset + (t_idx, h_idx, w_idx) in row-major grid order,
+ * offset = max(previous positions)+1; rope_delta = max position + 1 - length.
+ * seq_lens: host [n_seqs]; spans: host [n_spans] (any order, must not overlap or leave
+ * their sequence); pos_out: host [3, sum(seq_lens)] (t row, h row, w row);
+ * rope_delta_out: host [n_seqs]. Bit-exact integer arithmetic. */
+cc_status cc_build_mrope_positions(const cc_image_span* spans, int32_t n_spans,
+                                   const int32_t* seq_lens, int32_t n_seqs,
+                                   int32_t* pos_out, int32_t* rope_delta_out);
+
+/* Host helper: decode position of each sequence's new token, offset + rope_delta on all
+ * three axes (same paragraph). seq_lens/rope_delta host [batch]; pos_out host [3, batch]. */
+cc_status cc_build_decode_positions(const int32_t* seq_lens, const int32_t* rope_delta,
+                                    int32_t batch, int32_t* pos_out);
+
+/* Packs one layer's projection matrices into the w1/w2 layout of cc_layer_weights
+ * (device-to-device copies on `stream`). Inputs are the checkpoint's [out, in] matrices:
+ * wq [n_q d, H], wk/wv [n_kv d, H], wo [H, n_q d], wg/wu [I, H], wd [H, I].
+ * w1_out [N1, H] and w2_out [H, K2] are caller-allocated. Element size from cfg->dtype. */
+cc_status cc_pack_layer_weights(const cc_model_config* cfg, const void* wq, const void* wk,
+                                const void* wv, const void* wo, const void* wg,
+                                const void* wu, const void* wd, void* w1_out, void* w2_out,
+                                void* stream);
+
+/* Creates a plan: copies cfg and layer_types, borrows the weights (layers[num_layers],
+ * final_ln_w [H], embed [V, H], the tied embedding used as the LM head), allocates its
+ * device workspace for cfg->max_tokens tokens and builds the weight TMA descriptors.
+ * Uses the current CUDA device. On error *out is NULL. */
+cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_layer_weights* layers,
+                               const void* final_ln_w, const void* embed,
+                               cc_layer_plan** out);
+void cc_layer_plan_destroy(cc_layer_plan* plan);
+
+/* Prefill forward over packed sequences; updates hidden in place.
+ *  hidden      f32 [T, H] residual stream (input embeddings in, final h out; not normed)
+ *  pos_thw     int32 [3, T] position ids (cc_build_mrope_positions)
+ *  cu_seqlens  int32 [n_seqs + 1], cu_seqlens[0] = 0, non-decreasing, last = T
+ *  ds_rows     int32 [n_ds_rows] token rows of the image tokens (distinct), may be NULL
+ *              when n_deepstack == 0
+ *  ds_feats    host array of n_deepstack device pointers, each [n_ds_rows, H] in the
+ *              plan's dtype; tensor i is added after layer i (n_deepstack <= num_layers)
+ *  kv          optional paged cache to fill with every token's K/V (NULL: none);
+ *  page_table  int32 [n_seqs, max_pages] when kv is given
+ * T <= max_tokens. The last CTA of every row-tile is bounded by T; no host sync. */
+cc_status cc_prefill_forward(cc_layer_plan* plan, float* hidden, const int32_t* pos_thw,
+                             const int32_t* cu_seqlens, int32_t n_seqs, int32_t total_tokens,
+                             const int32_t* ds_rows, int32_t n_ds_rows,
+                             const void* const* ds_feats, int32_t n_deepstack,
+                             const cc_kv_pool* kv, const int32_t* page_table,
+                             int32_t max_pages, void* stream);
+
+/* One decode step: one new token per sequence.
+ *  hidden    f32 [batch, H] (in: the new tokens' embeddings; out: final h)
+ *  pos_thw   int32 [3, batch] (cc_build_decode_positions)
+ *  seq_lens  int32 [batch] tokens already cached; the new token's K/V are written at
+ *            slot seq_lens[b] and it attends over seq_lens[b] + 1 keys (sliding layers:
+ *            the last sliding_window of them). seq_lens[b] + 1 <= max_pages * page_size.
+ *  page_table int32 [batch, max_pages]; kv the cache (required). The caller advances
+ *  seq_lens afterwards. */
+cc_status cc_decode_step(cc_layer_plan* plan, float* hidden, const int32_t* pos_thw,
+                         const int32_t* seq_lens, const int32_t* page_table,
+                         int32_t max_pages, int32_t batch, const cc_kv_pool* kv,
+                         void* stream);
+
+/* Tied LM head: logits[r] = logit_scale * (LayerNorm_f(hidden[rows[r]]) @ embed^T).
+ * hidden f32 [*, H]; rows int32 [n_rows] (NULL: rows 0..n_rows-1); logits f32 [n_rows, V].
+ * n_rows <= max_tokens. */
+cc_status cc_logits(cc_layer_plan* plan, const float* hidden, const int32_t* rows,
+                    int32_t n_rows, float* logits, void* stream);
+
+/* Waits for `stream`, then returns and clears the plan's sticky device error flag
+ * (CC_ERR_TIMEOUT / CC_ERR_DEVICE_CHECK), or CC_ERR_CUDA if the stream failed. */
+cc_status cc_sync(cc_layer_plan* plan, void* stream);
+
+/* Per-kernel timing of a plan's calls (no counterpart on the pages; a measurement aid).
+ * While enabled, every kernel launch of cc_prefill_forward / cc_decode_step / cc_logits is
+ * bracketed by CUDA events recorded on the launching stream. cc_profile_read waits for
+ * those events and returns, per kernel class, the launch count and summed device time;
+ * it then clears the records. Enabling costs two event records per launch. */
+typedef enum {
+  CC_K_ROPE_TABLE = 0,     /* MRoPE cos/sin table                                   */
+  CC_K_ROW_MAPS = 1,       /* deepstack row map, KV slots, attention tile lists      */
+  CC_K_LAYERNORM = 2,      /* pre-block and final LayerNorm                          */
+  CC_K_GEMM_QKV_MLP = 3,   /* [q|k|v|gate,up] projection + rotation + SwiGLU epilogue */
+  CC_K_ATTN_PREFILL = 4,   /* causal / sliding flash attention                       */
+  CC_K_GEMM_OUT = 5,       /* [o|down] projection + residual (+ deepstack)           */
+  CC_K_ATTN_DECODE = 6,    /* paged decode attention + split combine                 */
+  CC_K_GEMM_HEAD = 7,      /* tied head x logit_scale                                */
+  CC_K_F32_PATH = 8,       /* kernels of the fp32 variant                            */
+  CC_K_COUNT = 9
+} cc_kernel_class;
+
+typedef struct {
+  int32_t launches;
+  double total_ms;
+} cc_kernel_time;
+
+cc_status cc_profile_enable(cc_layer_plan* plan, int32_t enable);
+/* out: CC_K_COUNT entries indexed by cc_kernel_class. */
+cc_status cc_profile_read(cc_layer_plan* plan, cc_kernel_time* out);
+const char* cc_kernel_class_name(int32_t kernel_class);
+
+/* ------------------------------- single operations ---------------------------------
+ * The steps of the path as separate calls, for composition and testing. They use a
+ * library-wide device error flag read by cc_op_sync. Scratch memory they need is
+ * taken with cudaMallocAsync/cudaFreeAsync on `stream`. */
+
+/* LayerNorm (Compass issue, "Text decoder forward": weight only, no bias, f32 statistics,
+ * biased variance, eps inside the square root): out[r] = bf16(gamma * (x[src] - mean) /
+ * sqrt(var + eps)), src = row_idx ? row_idx[r] : r. x f32 [*, H]; gamma bf16 [H];
+ * out bf16 [rows, H]. H % 128 == 0. */
+cc_status cc_op_layernorm(const float* x, const void* gamma, void* out, int32_t rows,
+                          int32_t hidden, float eps, const int32_t* row_idx, void* stream);
+
+/* Interleaved MRoPE cos/sin table (Compass issue, "Text decoder forward", interleaved
+ * MRoPE paragraph): table[t, j] = (cos, sin)(pos[axis(j), t] * theta^(-2j/head_dim)) for
+ * j < head_dim/2, axis(j) = h if j%3==1 and j<3*section[1], w if j%3==2 and
+ * j<3*section[2], else t. pos int32 [3, T]; table f32 [T, head_dim/2, 2]. */
+cc_status cc_op_mrope_table(const int32_t* pos, int32_t tokens, int32_t head_dim,
+                            double theta, const int32_t* section_host, float* table,
+                            void* stream);
+
+/* Dense bf16 GEMM on the tcgen05 tensor cores: C[M, N] = alpha * A[M, K] @ B[N, K]^T
+ * (+ C when accumulate != 0). A, B bf16 row-major (K contiguous); C f32 [M, N].
+ * K % 64 == 0, N % 128 == 0; A and B 16-byte aligned. */
+cc_status cc_op_gemm_bf16(const void* a, const void* b, float* c, int32_t m, int32_t n,
+                          int32_t k, float alpha, int32_t accumulate, void* stream);
+
+/* Prefill attention (causal, or sliding window when window > 0) over packed sequences,
+ * grouped-query, scale head_dim^-0.5, on the tcgen05 tensor cores.
+ * q bf16 [T, n_q * 128]; k, v bf16 [T, n_kv * 128]; out bf16 rows of leading dimension
+ * ld_out (head h at columns h*128 .. h*128+127). head_dim must be 128. */
+cc_status cc_op_attention_prefill(const void* q, const void* k, const void* v, void* out,
+                                  int32_t ld_out, const int32_t* cu_seqlens, int32_t n_seqs,
+                                  int32_t tokens, int32_t n_q, int32_t n_kv, int32_t window,
+                                  void* stream);
+
+/* Decode attention of one query token per sequence over a paged cache (split-KV):
+ * q bf16 [batch, n_q * 128]; k_pool, v_pool bf16 [n_pages, n_kv, page_size, 128];
+ * page_table int32 [batch, max_pages] (ids outside [0, n_pages) set the device flag
+ * CC_ERR_DEVICE_CHECK and their keys are skipped); n_keys int32 [batch] keys to attend
+ * over (token n_keys-1 is the query's own, n_keys <= max_pages * page_size);
+ * window > 0: only the last `window` keys; out bf16 rows of leading dimension ld_out.
+ * page_size must be 16 and n_q / n_kv one of 1, 2, 4, 8 (else CC_ERR_UNSUPPORTED). */
+cc_status cc_op_attention_decode(const void* q, const void* k_pool, const void* v_pool,
+                                 int32_t n_pages, const int32_t* page_table, int32_t max_pages,
+                                 const int32_t* n_keys, int32_t batch, int32_t n_q,
+                                 int32_t n_kv, int32_t page_size, int32_t window, void* out,
+                                 int32_t ld_out, void* stream);
+
+/* Waits for `stream`; returns and clears the library-wide device error flag of the
+ * single operations. */
+cc_status cc_op_sync(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* CC_H_ */

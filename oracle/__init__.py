@@ -5,3 +5,4 @@ bench's CPU-baseline leg, never by the library. It shares no code with the CUDA 
 """
 from .decoder import *  # noqa: F401,F403
 from . import decoder  # noqa: F401
+from . import runs  # noqa: F401,E402

@@ -89,6 +89,8 @@ def rope_index(seq_len: int, images):
             pos[:, k] = nxt
             nxt += 1
             k += 1
+    if seq_len == 0:          # no positions: rope_delta taken as 0 (max+1 - L with max = -1)
+        return pos, 0
     return pos, int(pos.max()) + 1 - seq_len
 
 

@@ -1,0 +1,40 @@
+"""Runs the oracle over a whole workload. TEST INFRASTRUCTURE ONLY (see oracle/__init__).
+
+``inp`` is any object with the fields of synth.Inputs; positions are computed here by
+the oracle's own rule, never taken from the CUDA path.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import decoder as O
+
+
+def run_prefill(inp, mirror_bf16=None, return_all=False):
+    """Final residual stream h [T, H] and logits of the head rows, both float64."""
+    wl = inp.wl
+    shape = O.shape_dict(inp.shape)
+    if mirror_bf16 is None:
+        mirror_bf16 = inp.shape.dtype == "bf16"
+    spans = [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w) for i in inp.images]
+    pos, _ = O.positions(wl.seq_lens, spans)
+    ds = [inp.ds(i) for i in range(wl.n_deepstack)]
+    out = O.prefill(inp.hidden, inp.layer, shape, pos, inp.cu_seqlens, inp.ds_rows, ds,
+                    mirror_bf16, return_all=return_all)
+    h, hs = (out if return_all else (out, None))
+    logits = O.logits(h[inp.head_rows], inp.final_ln, inp.embed, shape, mirror_bf16)
+    return (h, logits, hs) if return_all else (h, logits)
+
+
+def run_decode(inp, mirror_bf16=True):
+    shape = O.shape_dict(inp.shape)
+    h = O.decode_step(inp.hidden, inp.layer, shape, inp.seq_lens, inp.rope_delta, inp.page_table,
+                      inp.kv, inp.wl.page_size, mirror_bf16)
+    logits = O.logits(h[inp.head_rows], inp.final_ln, inp.embed, shape, mirror_bf16)
+    return h, logits
+
+
+def run(inp, mirror_bf16=None):
+    if inp.wl.mode == "decode":
+        return run_decode(inp, True if mirror_bf16 is None else mirror_bf16)
+    return run_prefill(inp, mirror_bf16)

@@ -1,0 +1,190 @@
+"""Parity of the single CUDA operations (through the C-ABI) against the fp64 oracle.
+
+Inputs are seeded; sizes span several tiles and end in ragged tails. Tolerances:
+LayerNorm and the MRoPE table are compared at their storage precision; the GEMM at fp32
+accumulation accuracy; attention (bf16 P and bf16 output) within the stack tolerance
+max-abs 2e-2 / mean-abs 2e-3 (tighter in practice).
+"""
+import numpy as np
+import pytest
+import torch
+
+import cohere_compass_decoder_gb300._lib as L
+from oracle import decoder as O
+
+from gpu_util import require_gpu, bf16_dev, f64, err_stats, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _sync():
+    torch.cuda.synchronize()
+    L.cc_op_sync()
+
+
+# --------------------------------------------------------------------------- LayerNorm
+@pytest.mark.parametrize("rows,H", [(300, 2048), (5, 256), (129, 1024)])
+def test_layernorm_matches_oracle(rows, H):
+    rng = np.random.default_rng(rows + H)
+    x = (rng.standard_normal((rows + 7, H)) * 3 + 0.5).astype(np.float32)
+    g = bf16_dev(1 + 0.02 * rng.standard_normal(H))
+    idx = rng.permutation(rows + 7)[:rows].astype(np.int32)
+    out = torch.empty(rows, H, dtype=torch.bfloat16, device="cuda")
+    xd = torch.from_numpy(x).cuda()
+    L.cc_op_layernorm(xd, g, out, rows, H, 1e-5, torch.from_numpy(idx).cuda())
+    _sync()
+    want = O.round_bf16(O.layer_norm(x[idx].astype(np.float64), f64(g), 1e-5))
+    got = f64(out)
+    ulp = np.abs(want) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(got - want) <= ulp * 1.01)
+    assert np.mean(got != want) < 0.01
+
+
+# --------------------------------------------------------------------------- MRoPE table
+@pytest.mark.parametrize("section,theta", [((24, 20, 20), 50000.0), ((12, 10, 10), 1e4)])
+def test_mrope_table_matches_oracle(section, theta):
+    rng = np.random.default_rng(3)
+    T = 777
+    pos = rng.integers(0, 40000, size=(3, T)).astype(np.int32)
+    d = 2 * sum(section)
+    table = torch.empty(T, d // 2, 2, dtype=torch.float32, device="cuda")
+    L.cc_op_mrope_table(torch.from_numpy(pos).cuda(), T, d, theta, section, table)
+    _sync()
+    cos, sin = O.mrope_cos_sin(pos, d, theta, section)
+    got = f64(table)
+    assert np.abs(got[..., 0] - cos[:, :d // 2]).max() < 2e-6
+    assert np.abs(got[..., 1] - sin[:, :d // 2]).max() < 2e-6
+
+
+# --------------------------------------------------------------------------- GEMM
+@pytest.mark.parametrize("m,n,k", [(128, 128, 64), (300, 384, 640), (64, 2560, 2048),
+                                   (1, 1280, 128), (1000, 512, 1024)])
+def test_gemm_matches_oracle(m, n, k):
+    rng = np.random.default_rng(m * 7 + n + k)
+    a = bf16_dev(rng.standard_normal((m, k)))
+    b = bf16_dev(rng.standard_normal((n, k)))
+    c = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    L.cc_op_gemm_bf16(a, b, c, m, n, k, 0.5, 0)
+    _sync()
+    want = 0.5 * (f64(a) @ f64(b).T)
+    got = f64(c)
+    rel = np.abs(got - want).max() / np.abs(want).max()
+    assert np.all(np.isfinite(got))
+    assert rel < 1e-5, rel
+
+
+def test_gemm_accumulates():
+    rng = np.random.default_rng(11)
+    m, n, k = 200, 256, 512
+    a, b = bf16_dev(rng.standard_normal((m, k))), bf16_dev(rng.standard_normal((n, k)))
+    c0 = rng.standard_normal((m, n)).astype(np.float32)
+    c = torch.from_numpy(c0).cuda()
+    L.cc_op_gemm_bf16(a, b, c, m, n, k, 1.0, 1)
+    _sync()
+    want = c0 + f64(a) @ f64(b).T
+    assert np.abs(f64(c) - want).max() / np.abs(want).max() < 1e-5
+
+
+# --------------------------------------------------------------------------- prefill attention
+def _attn_case(lens, nq, nkv, window, seed):
+    rng = np.random.default_rng(seed)
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = bf16_dev(rng.standard_normal((T, nq * 128)))
+    k = bf16_dev(rng.standard_normal((T, nkv * 128)))
+    v = bf16_dev(rng.standard_normal((T, nkv * 128)))
+    ld = nq * 128 + 64
+    out = torch.full((T, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.cc_op_attention_prefill(q, k, v, out, ld, torch.from_numpy(cu).cuda(), len(lens), T, nq,
+                              nkv, window)
+    _sync()
+    want = O.attention(f64(q).reshape(T, nq, 128), f64(k).reshape(T, nkv, 128),
+                       f64(v).reshape(T, nkv, 128), cu, window if window > 0 else None,
+                       128 ** -0.5)
+    got = f64(out)[:, :nq * 128].reshape(T, nq, 128)
+    assert np.all(np.isnan(f64(out)[:, nq * 128:]))   # nothing written past the heads
+    return got, want
+
+
+@pytest.mark.parametrize("lens,nq,nkv,window", [
+    ([300], 4, 2, 0),
+    ([300], 4, 1, 64),
+    ([100, 260, 37], 2, 2, 100),
+    ([1], 2, 1, 0),
+    ([1000], 16, 4, 512),
+    ([129, 128, 127], 8, 1, 0),
+])
+def test_attention_prefill_matches_oracle(lens, nq, nkv, window):
+    got, want = _attn_case(lens, nq, nkv, window, seed=sum(lens) + nq + window)
+    assert_close(got, want, 2e-2, 2e-3, "attention")
+
+
+def test_attention_window_at_least_sequence_equals_full():
+    rng = np.random.default_rng(5)
+    T, nq, nkv = 333, 4, 2
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    q, k, v = (bf16_dev(rng.standard_normal((T, n * 128))) for n in (nq, nkv, nkv))
+    outs = []
+    for w in (0, T, 5000):
+        o = torch.empty(T, nq * 128, dtype=torch.bfloat16, device="cuda")
+        L.cc_op_attention_prefill(q, k, v, o, nq * 128, cu, 1, T, nq, nkv, w)
+        outs.append(o)
+    _sync()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+# --------------------------------------------------------------------------- decode attention
+@pytest.mark.parametrize("nq,nkv,window", [(8, 2, 0), (8, 2, 200), (16, 4, 0), (4, 4, 37),
+                                           (8, 1, 0)])
+def test_attention_decode_matches_oracle(nq, nkv, window):
+    rng = np.random.default_rng(nq * 13 + nkv + window)
+    B, ps, max_pages = 7, 16, 44
+    n_pages = B * max_pages + 5
+    n_keys = rng.integers(1, max_pages * ps + 1, size=B).astype(np.int32)
+    n_keys[0] = 1
+    n_keys[1] = max_pages * ps
+    table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    kp = bf16_dev(rng.standard_normal((n_pages, nkv, ps, 128)))
+    vp = bf16_dev(rng.standard_normal((n_pages, nkv, ps, 128)))
+    q = bf16_dev(rng.standard_normal((B, nq * 128)))
+    out = torch.empty(B, nq * 128, dtype=torch.bfloat16, device="cuda")
+    L.cc_op_attention_decode(q, kp, vp, n_pages, torch.from_numpy(table).cuda(), max_pages,
+                             torch.from_numpy(n_keys).cuda(), B, nq, nkv, ps, window, out,
+                             nq * 128)
+    _sync()
+    K, V, Q = f64(kp), f64(vp), f64(q).reshape(B, nq, 128)
+    want = np.zeros((B, nq, 128))
+    for b in range(B):
+        n = int(n_keys[b])
+        idx = np.arange(n)
+        Kb = K[table[b][idx // ps], :, idx % ps, :]
+        Vb = V[table[b][idx // ps], :, idx % ps, :]
+        qi = np.zeros((n, nq, 128))
+        qi[n - 1] = Q[b]
+        want[b] = O.attention(qi, Kb, Vb, [0, n], window if window > 0 else None,
+                              128 ** -0.5, row_block=n)[n - 1]
+    got = f64(out).reshape(B, nq, 128)
+    assert_close(got, want, 2e-2, 2e-3, "decode attention")
+
+
+def test_attention_decode_flags_bad_page_ids():
+    B, nq, nkv, ps, max_pages = 2, 4, 1, 16, 4
+    n_pages = 8
+    table = torch.tensor([[0, 1, 2, 3], [4, 5, 99, 7]], dtype=torch.int32, device="cuda")
+    kp = torch.zeros(n_pages, nkv, ps, 128, dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    q = torch.zeros(B, nq * 128, dtype=torch.bfloat16, device="cuda")
+    nk = torch.tensor([64, 64], dtype=torch.int32, device="cuda")
+    out = torch.empty(B, nq * 128, dtype=torch.bfloat16, device="cuda")
+    L.cc_op_attention_decode(q, kp, vp, n_pages, table, max_pages, nk, B, nq, nkv, ps, 0, out,
+                             nq * 128)
+    torch.cuda.synchronize()
+    with pytest.raises(L.CCError) as e:
+        L.cc_op_sync()
+    assert e.value.status == L.CC_ERR_DEVICE_CHECK
+    L.cc_op_sync()   # the flag was cleared

@@ -1,0 +1,169 @@
+"""Parity of the whole path (layer stack + head, through the C-ABI) against the oracle.
+
+bf16 workloads compare against the oracle's bf16-mirror mode (rounding at the GPU's
+storage points) with the benchmark spec's tolerance on the outputs: max-abs <= 2e-2 and
+mean-abs <= 2e-3 on the final hidden state and on the logits; the logits also have to
+agree to 2% of their largest magnitude, which is the stricter test for them. The fp32
+workload compares against pure fp64 at fp32-level tolerance (1e-4).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import runs as R
+from synth import Inputs, Workload, ImageSpan, small_shape, SLIDING, FULL
+from synth.configs import cfg1, cfg2, cfg3, cfg4, cfg5
+from cohere_compass_decoder_gb300.workload import GpuWorkload, as_numpy
+
+from gpu_util import require_gpu, assert_close, err_stats
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX, TOL_MEAN = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _check(inp, gw, h_gpu, lg_gpu, tol=(TOL_MAX, TOL_MEAN), lg_rel=2e-2):
+    h_ref, lg_ref = R.run(inp)
+    h = as_numpy(h_gpu)
+    lg = as_numpy(lg_gpu)
+    mx, mn = assert_close(h, h_ref, tol[0], tol[1], "hidden")
+    lmx, lmn = assert_close(lg, lg_ref, tol[0], tol[1], "logits")
+    rel = lmx / max(np.abs(lg_ref).max(), 1e-30)
+    assert rel <= lg_rel, f"logits relative error {rel:.3g}"
+    return dict(h_max=mx, h_mean=mn, lg_max=lmx, lg_mean=lmn, lg_rel=rel)
+
+
+def _run(inp, max_tokens=None):
+    gw = GpuWorkload(inp, max_tokens=max_tokens)
+    h = gw.fresh_hidden()
+    lg = gw.step(h)
+    gw.sync()
+    return gw, h, lg
+
+
+def _small(name, seq_lens, images, n_ds, types=(SLIDING, FULL), window=64, head_rows="all",
+           seed=21, **kw):
+    shape = small_shape(num_layers=len(types), layer_types=types, window=window, **kw)
+    return Inputs(Workload(name, shape, "prefill", seq_lens, images=images, n_deepstack=n_ds,
+                           head_rows=head_rows, seed=seed))
+
+
+# ------------------------------------------------------------------------- small bf16 stacks
+def test_small_stack_single_sequence():
+    inp = _small("small1", [300], [ImageSpan(0, 37, 1, 8, 8)], 2)
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
+def test_small_stack_varlen_and_gqa_variants():
+    imgs = [ImageSpan(0, 10, 1, 5, 6), ImageSpan(1, 0, 1, 4, 4), ImageSpan(2, 50, 1, 3, 3),
+            ImageSpan(2, 70, 1, 2, 5)]
+    inp = _small("small2", [100, 200, 157], imgs, 2, types=(SLIDING, SLIDING, FULL, SLIDING),
+                 window=90, heads=(8, 2), hidden=384, inter=256, vocab=384, seed=22)
+    gw, h, lg = _run(inp, max_tokens=600)
+    _check(inp, gw, h, lg)
+
+
+def test_small_stack_mha_and_no_images():
+    inp = _small("small3", [130], [], 0, types=(FULL, SLIDING), window=33, heads=(2, 2),
+                 hidden=128, inter=128, vocab=256, seed=23)
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
+def test_causal_prefix_on_gpu():
+    """First 48 logits of a 96-token prefill equal those of a 48-token prefill (pages'
+    text_prefill_is_causal), here on the GPU path (3 sliding + 1 full layer)."""
+    types = (SLIDING, SLIDING, SLIDING, FULL)
+    a = _small("c96", [96], [], 0, types=types, window=20, head_rows="all", seed=24)
+    b = _small("c48", [48], [], 0, types=types, window=20, head_rows="all", seed=24)
+    _, ha, la = _run(a)
+    _, hb, lb = _run(b)
+    mx, _ = err_stats(as_numpy(la)[:48], as_numpy(lb))
+    assert mx <= 1e-4, mx
+
+
+# ------------------------------------------------------------------------- the five workloads
+def test_cfg1_single_layer_fp32():
+    inp = Inputs(cfg1())
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg, tol=(1e-4, 1e-5), lg_rel=1e-4)
+
+
+def test_cfg2_two_layer_pair():
+    inp = Inputs(cfg2())
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
+def _small_decode(seed=31, B=5, types=(SLIDING, FULL), window=70, heads=(8, 2)):
+    shape = small_shape(num_layers=len(types), layer_types=types, window=window, heads=heads)
+    wl = Workload("dec_small", shape, "decode", [], head_rows="all", seed=seed, decode_batch=B,
+                  cache_len=150, page_size=16)
+    return Inputs(wl)
+
+
+def test_small_decode_step():
+    inp = _small_decode()
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
+def test_cfg4_decode_step():
+    inp = Inputs(cfg4())
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
+def test_decode_continues_prefill_on_gpu():
+    """Prefill of L tokens fills the paged cache; decoding token L+1 then matches the last
+    row of an (L+1)-token prefill (both on the GPU)."""
+    import cohere_compass_decoder_gb300._lib as L
+    types = (SLIDING, FULL, SLIDING)
+    Lc = 77
+    full = _small("dcp_full", [Lc + 1], [ImageSpan(0, 10, 1, 3, 4)], 0, types=types, window=40,
+                  head_rows="all", seed=41)
+    gw_full, h_full, lg_full = _run(full)
+    # same weights and inputs, first Lc tokens only, with a paged cache
+    pre = _small("dcp_pre", [Lc], [ImageSpan(0, 10, 1, 3, 4)], 0, types=types, window=40,
+                 head_rows="all", seed=41)
+    gw = GpuWorkload(pre, max_tokens=Lc + 1)
+    ps, max_pages = 16, (Lc + 1 + 15) // 16
+    n_pages = max_pages + 3
+    table = torch.tensor(np.random.default_rng(1).permutation(n_pages)[:max_pages][None, :],
+                         dtype=torch.int32, device="cuda")
+    shape = pre.shape
+    kp = [torch.zeros(n_pages, shape.num_key_value_heads, ps, 128, dtype=torch.bfloat16,
+                      device="cuda") for _ in types]
+    vp = [torch.zeros_like(t) for t in kp]
+    kv = L.make_kv_pool(kp, vp, n_pages)
+    h = gw.fresh_hidden()
+    gw.prefill(h, kv=kv, page_table=table, max_pages=max_pages)
+    # the decode token: the (Lc+1)-th input row, position from rope_delta
+    x = torch.from_numpy(full.hidden[Lc:Lc + 1].copy()).cuda()
+    _, delta = L.cc_build_mrope_positions([(0, 10, 1, 3, 4)], [Lc])
+    pos = torch.tensor(L.cc_build_decode_positions([Lc], delta), dtype=torch.int32, device="cuda")
+    seq_lens = torch.tensor([Lc], dtype=torch.int32, device="cuda")
+    gw.stack.decode(x, pos, seq_lens, table, max_pages, kv)
+    gw.sync()
+    mx, mn = err_stats(as_numpy(x)[0], as_numpy(h_full)[Lc])
+    assert mx <= TOL_MAX and mn <= TOL_MEAN, (mx, mn)
+
+
+@pytest.mark.slow
+def test_cfg3_stack28():
+    inp = Inputs(cfg3())
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
+@pytest.mark.slow
+def test_cfg5_varlen():
+    inp = Inputs(cfg5())
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
