@@ -23,7 +23,7 @@ EXPORTS = [
     "cc_prefill_forward", "cc_decode_step", "cc_logits", "cc_sync", "cc_op_layernorm",
     "cc_op_mrope_table", "cc_op_gemm_bf16", "cc_op_attention_prefill",
     "cc_op_attention_decode", "cc_op_sync", "cc_profile_enable", "cc_profile_read",
-    "cc_kernel_class_name",
+    "cc_kernel_class_name", "cc_op_attention_decode_noalloc",
 ]
 KERNEL_CLASSES = ["rope_table", "row_maps", "layernorm", "gemm_qkv_mlp", "attn_prefill",
                   "gemm_out_resid", "attn_decode", "gemm_head", "f32_path"]
@@ -99,6 +99,8 @@ def lib() -> C.CDLL:
             "cc_op_attention_decode": (C.c_int, [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32,
                                                  i32, i32, vp, i32, vp]),
             "cc_op_sync": (C.c_int, [vp]),
+            "cc_op_attention_decode_noalloc": (C.c_int, [vp, vp, vp, i32, vp, i32, vp, i32, i32,
+                                                         i32, i32, i32, vp, i32, vp, vp]),
             "cc_profile_enable": (C.c_int, [vp, i32]),
             "cc_profile_read": (C.c_int, [vp, C.POINTER(cc_kernel_time)]),
             "cc_kernel_class_name": (C.c_char_p, [i32]),
@@ -289,6 +291,17 @@ def cc_op_attention_decode(q, k_pool, v_pool, n_pages, page_table, max_pages, n_
                                         _ptr(page_table), max_pages, _ptr(n_keys), batch, n_q, n_kv,
                                         page_size, window, _ptr(out), ld_out, _stream(stream)),
            "cc_op_attention_decode")
+
+
+def cc_op_attention_decode_noalloc(q, k_pool, v_pool, n_pages, page_table, max_pages, n_keys,
+                                   batch, n_q, n_kv, page_size, window, out, ld_out,
+                                   err_flag=None, stream=None):
+    """Decode attention with the library's fixed scratch: allocates no device memory."""
+    _check(lib().cc_op_attention_decode_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), n_pages,
+                                                _ptr(page_table), max_pages, _ptr(n_keys), batch,
+                                                n_q, n_kv, page_size, window, _ptr(out), ld_out,
+                                                _ptr(err_flag), _stream(stream)),
+           "cc_op_attention_decode_noalloc")
 
 
 # ------------------------------------------------------------------------ profiling

@@ -15,6 +15,8 @@
 // heads. Online softmax per head in the log2 domain; the warps' partial results merge in
 // shared memory and the split's (max, sum, unnormalised O) goes to scratch.
 // Kernel 2 merges the splits of each (sequence, head) and writes O as bf16.
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -354,4 +356,61 @@ cc_status launch_attn_decode(const __nv_bfloat16* q, int ld_q, const __nv_bfloat
   return CC_OK;
 }
 
+// ------------------------------------------------------------ no-allocation variant
+// Fixed split-KV scratch for callers that cannot allocate: 4 Mi floats (16 MiB) per GPU.
+// Every split either writes its partial (max, sum, O) or marks itself empty (max = -inf),
+// and the combine reads only the splits of the current call, so nothing needs clearing.
+constexpr size_t kNoAllocScratchFloats = size_t(1) << 22;
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per device.
+static cc_status noalloc_scratch(float** out) {
+  static std::mutex mu;
+  static float* addr[kNoAllocMaxDevices] = {};
+  int dev = 0;
+  CC_CHECK_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return CC_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      last_cuda_error() = e;
+      return CC_ERR_CUDA;
+    }
+    addr[dev] = static_cast<float*>(p);
+  }
+  *out = addr[dev];
+  return CC_OK;
+}
+
 }  // namespace cc
+
+extern "C" cc_status cc_op_attention_decode_noalloc(const void* q, const void* k_pool,
+                                                    const void* v_pool, int32_t n_pages,
+                                                    const int32_t* page_table, int32_t max_pages,
+                                                    const int32_t* n_keys, int32_t batch,
+                                                    int32_t n_q, int32_t n_kv, int32_t page_size,
+                                                    int32_t window, void* out, int32_t ld_out,
+                                                    int32_t* err_flag, void* stream) {
+  using namespace cc;
+  if (batch < 0 || n_q <= 0 || n_kv <= 0 || n_q % n_kv || max_pages <= 0 || window < 0 ||
+      page_size <= 0 || ld_out < n_q * 128 || n_pages <= 0)
+    return CC_ERR_INVALID_ARG;
+  if (batch == 0) return CC_OK;
+  if (!q || !k_pool || !v_pool || !page_table || !n_keys || !out) return CC_ERR_INVALID_ARG;
+  if (decode_scratch_floats(batch, n_q, max_pages) > kNoAllocScratchFloats)
+    return CC_ERR_INVALID_ARG;
+  float* scratch = nullptr;
+  CC_CHECK_STATUS(noalloc_scratch(&scratch));
+  DecodeScratch scr;
+  scr.part_o = scratch;
+  scr.part_ml = scratch + (size_t)batch * n_q * decode_splits(max_pages) * 128;
+  return launch_attn_decode(static_cast<const __nv_bfloat16*>(q), n_q * 128,
+                            static_cast<const __nv_bfloat16*>(k_pool),
+                            static_cast<const __nv_bfloat16*>(v_pool), n_pages, page_table,
+                            max_pages, n_keys, batch, n_q, n_kv, page_size, window, scr,
+                            static_cast<__nv_bfloat16*>(out), ld_out, err_flag,
+                            static_cast<cudaStream_t>(stream));
+}

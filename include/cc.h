@@ -271,6 +271,28 @@ cc_status cc_op_attention_decode(const void* q, const void* k_pool, const void* 
  * single operations. */
 cc_status cc_op_sync(void* stream);
 
+/* Decode attention that allocates no device memory. The pages have no counterpart to
+ * this call; it exists for callers that cannot call cudaMalloc: a serving runtime whose
+ * memory pool has already reserved the device (a fresh allocation fails or fragments it),
+ * a decode loop that must not take the device-wide synchronisation cudaMalloc/cudaFree
+ * may impose, or a host that is not allowed to allocate at all.
+ * Same inputs, outputs and result as cc_op_attention_decode. Its split-KV scratch is one
+ * fixed array inside the library (16 MiB, held on every GPU that loads the library until
+ * the process exits): it needs batch * n_q * ceil(max_pages / 16) * 130 floats, at most
+ * 4194304; larger problems return CC_ERR_INVALID_ARG and launch nothing.
+ * The first call on a device looks up that array's device address (with that device
+ * current) and caches it; make that first call before any stream capture. All calls share
+ * the array, so calls that may overlap on the GPU (other streams, other threads) race and
+ * must be serialised by the caller. err_flag: optional caller-owned device int32 that
+ * receives CC_ERR_TIMEOUT / CC_ERR_DEVICE_CHECK (first error wins; the caller clears it);
+ * NULL: device-side problems are not reported. */
+cc_status cc_op_attention_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                         int32_t n_pages, const int32_t* page_table,
+                                         int32_t max_pages, const int32_t* n_keys, int32_t batch,
+                                         int32_t n_q, int32_t n_kv, int32_t page_size,
+                                         int32_t window, void* out, int32_t ld_out,
+                                         int32_t* err_flag, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
