@@ -46,6 +46,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-prefill", action="store_true", help="decode leg only (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=0,
@@ -391,7 +392,7 @@ def main():
     pk = peaks()
     clocks = Clocks(dist.local) if dist.rank == 0 else None
     t_start = time.time()
-    pre = prefill_leg(args, dist, pk)
+    pre = None if args.no_prefill else prefill_leg(args, dist, pk)
     dec = None if args.no_decode else decode_leg(args, dist, pk)
     # keep the clock sampler running for at least ~1 s of GPU work
     if clocks and time.time() - t_start < 1.5:
@@ -401,7 +402,9 @@ def main():
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, args.cpu_tokens)
         cpu.pop("seconds", None)
-    if dist.rank == 0:
+    if dist.rank == 0 and pre is None:
+        print(json.dumps({"decode": dec}))
+    elif dist.rank == 0:
         line = {
             "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"] / args.steps,

@@ -224,7 +224,7 @@ static cc_status check_config(const cc_model_config* c) {
     if (c->head_dim != 128 || c->vocab_size % 128 != 0 || c->kv_page_size != 16)
       return CC_ERR_UNSUPPORTED;
     const int g = c->n_q_heads / c->n_kv_heads;
-    if (g != 1 && g != 2 && g != 4 && g != 8) return CC_ERR_UNSUPPORTED;
+    if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return CC_ERR_UNSUPPORTED;
   } else {
     if (c->head_dim > 128) return CC_ERR_UNSUPPORTED;
   }
@@ -380,14 +380,14 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
   if (kv)
     CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_prefill(cu, n_seqs, T, page_table, max_pages, c.kv_page_size,
                                             kv->n_pages, p->kv_slot, p->err, s));
-  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, c.sliding_window, p->tiles_s, p->n_tiles, s));
-  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, 0, p->tiles_f, p->n_tiles + 1, s));
+  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, c.sliding_window, p->tiles_s, p->n_tiles, s));
+  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, 0, p->tiles_f, p->n_tiles + 1, s));
   CUtensorMap ta, ta2, tq, tk, tv;
   if (!make_tmap_bf16_2d(&ta, p->a, T, p->H, p->H, 128, 64) ||
       !make_tmap_bf16_2d(&ta2, p->a2, T, p->K2, p->K2, 128, 64) ||
       !make_tmap_bf16_2d(&tq, p->q, T, p->q_cols, p->q_cols, 128, 64) ||
-      !make_tmap_bf16_2d(&tk, p->k, T, p->kv_cols, p->kv_cols, 128, 64) ||
-      !make_tmap_bf16_2d(&tv, p->v, T, p->kv_cols, p->kv_cols, 128, 64))
+      !make_tmap_bf16_2d(&tk, p->k, T, p->kv_cols, p->kv_cols, attn_kv_box_rows(), 64) ||
+      !make_tmap_bf16_2d(&tv, p->v, T, p->kv_cols, p->kv_cols, attn_kv_box_rows(), 64))
     return CC_ERR_CUDA;
   const int tiles = attn_max_tiles(T, n_seqs);
   for (int i = 0; i < c.num_layers; ++i) {
@@ -653,8 +653,8 @@ extern "C" cc_status cc_op_attention_prefill(const void* q, const void* k, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   CUtensorMap tq, tk, tv;
   if (!make_tmap_bf16_2d(&tq, q, tokens, n_q * 128, n_q * 128, 128, 64) ||
-      !make_tmap_bf16_2d(&tk, k, tokens, n_kv * 128, n_kv * 128, 128, 64) ||
-      !make_tmap_bf16_2d(&tv, v, tokens, n_kv * 128, n_kv * 128, 128, 64))
+      !make_tmap_bf16_2d(&tk, k, tokens, n_kv * 128, n_kv * 128, attn_kv_box_rows(), 64) ||
+      !make_tmap_bf16_2d(&tv, v, tokens, n_kv * 128, n_kv * 128, attn_kv_box_rows(), 64))
     return CC_ERR_INVALID_ARG;
   const int max_tiles = attn_max_tiles(tokens, n_seqs);
   void* scratch = nullptr;
@@ -662,7 +662,7 @@ extern "C" cc_status cc_op_attention_prefill(const void* q, const void* k, const
   CC_CHECK_CUDA(cudaMallocAsync(&scratch, bytes, s));
   int32_t* n_tiles = static_cast<int32_t*>(scratch);
   AttnTile* tiles = reinterpret_cast<AttnTile*>(static_cast<uint8_t*>(scratch) + 256);
-  cc_status st = launch_attn_tiles(cu_seqlens, n_seqs, window, tiles, n_tiles, s);
+  cc_status st = launch_attn_tiles(cu_seqlens, n_seqs, tokens, window, tiles, n_tiles, s);
   if (st == CC_OK)
     st = launch_attn_prefill(tq, tk, tv, static_cast<__nv_bfloat16*>(out), ld_out, tiles, n_tiles,
                              max_tiles, n_q, n_kv, window, op_error_flag(), s);

@@ -13,8 +13,9 @@ namespace cc {
 // Device error codes written to the sticky error flag (same values as cc_status).
 enum : int { CC_DEV_TIMEOUT = CC_ERR_TIMEOUT, CC_DEV_CHECK = CC_ERR_DEVICE_CHECK };
 
-// A bounded inter-warp wait gives up after this long (no launch here runs for seconds).
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// A bounded inter-warp wait gives up after this many SM clock cycles (about 2 s at the
+// GB300's 2.07 GHz maximum clock; no launch here runs for seconds).
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 constexpr int kNumSMsFallback = 152;
 

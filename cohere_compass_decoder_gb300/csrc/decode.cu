@@ -1,19 +1,26 @@
-// Decode attention over a paged KV cache: one query token per sequence, split-KV.
+// Decode attention over a paged KV cache on the tcgen05 tensor cores: one query token per
+// sequence, split-KV.
 //
 // Definition: the new token of sequence b (query index n-1, n = n_keys[b]) attends over
 // keys 0..n-1 of its cache (full layers) or over the last `window` of them (sliding
 // layers), grouped-query, scale d^-0.5 (mlxcel issue "Cohere Compass /
-// North-Micro-Vision", section "Text decoder forward"; the cache layout is this
+// North-Micro-Vision", section "Text decoder forward"). The cache layout is this
 // library's: pool [page][kv_head][16 tokens][128], so one page of one KV head is a 4 KB
-// contiguous block).
+// contiguous block.
 //
-// Kernel 1 (grid: key splits x KV heads x batch, 4 warps): every warp streams its pages
-// (4 KB of K and 4 KB of V each) with cp.async.bulk into a private 3-slot shared ring, so
-// about 200 KB per SM are in flight. The G = n_q / n_kv query heads that share the KV head
-// are handled together: per step 8 lanes take one key (16 of its 128 dims each, 16-byte
-// shared loads that do not conflict), so each K/V byte is read from HBM once for all G
-// heads. Online softmax per head in the log2 domain; the warps' partial results merge in
-// shared memory and the split's (max, sum, unnormalised O) goes to scratch.
+// Kernel 1, one CTA per (key split, KV head, sequence), 6 warps:
+//   warp 0      TMA: the G query heads of the KV head (one 16-row box), then per tile of 128
+//               keys the 8 pages of K and of V, gathered through the page table straight
+//               into 128-byte-swizzled tiles (3-stage ring)
+//   warp 1      MMA: S^T = K Q^T (M = 128 keys, N = 16 query rows of which G are used) into
+//               one of two TMEM score buffers, then O^T += V^T P (V read MN-major as the A
+//               operand, P = [16 x 128 keys] bf16 in shared memory)
+//   warps 2..5  softmax, one key per thread: masked scores of its G heads from TMEM, the
+//               tile's per-head maximum through shuffles and shared memory, the running
+//               maximum moved (and O^T rescaled in TMEM) only when it grows by more than 2^8,
+//               p = 2^(s - m), per-thread partial sums, P into shared memory.
+// Each K/V byte is read from HBM once for all G query heads and every multiply runs on the
+// tensor cores, so the kernel streams HBM instead of issuing CUDA-core FMAs.
 // Kernel 2 merges the splits of each (sequence, head) and writes O as bf16.
 #include <mutex>
 
@@ -24,61 +31,112 @@ namespace cc {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kSlots = 3;
+constexpr int kThreads = 192;
 constexpr int kPage = 16;
-constexpr uint32_t kPageBytes = kPage * 128 * 2;       // 4 KB per page and head
-constexpr uint32_t kSlotBytes = 2 * kPageBytes;        // K and V
-constexpr int kPagesPerSplit = 16;
+constexpr int kTileKeys = 128;
+constexpr int kPagesPerTile = kTileKeys / kPage;   // 8
+constexpr int kTilesPerSplit = 8;                  // 1024 keys per CTA
+constexpr int kPagesPerSplit = kPagesPerTile * kTilesPerSplit;
+constexpr int kStages = 3;
+constexpr int kQRows = 16;                         // MMA N (query heads, padded)
+constexpr uint32_t kTile = kTileKeys * 128 * 2;    // 32 KB: 128 keys x 128 dims
+constexpr uint32_t kHalf = kTileKeys * 64 * 2;     // one 64-dim box column: 16 KB
+constexpr uint32_t kQBytes = kQRows * 128 * 2;     // 4 KB
+constexpr uint32_t kPBytes = kQRows * kTileKeys * 2;   // 4 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = 4096;                   // 1024-aligned
+constexpr uint32_t kOffV = kOffK + kStages * kTile;
+constexpr uint32_t kOffP = kOffV + kStages * kTile;
+constexpr uint32_t kOffRed = kOffP + 2 * kPBytes;  // [2][4 warps][16] floats
+constexpr uint32_t kOffBar = kOffRed + 2 * 4 * 16 * 4;
+constexpr size_t kSmem = 1024 + kOffBar + 256;
+constexpr uint32_t kTmemCols = 64;                 // S0 | S1 | O (16 columns each)
+constexpr uint32_t kIdescS = idesc_bf16(128, kQRows, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, kQRows, 0) | (1u << 15);   // A MN-major
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.0f;
 
-template <int G>
-struct DecSmem {
-  static constexpr uint32_t kRing = kWarps * kSlots * kSlotBytes;      // 96 KB
-  static constexpr uint32_t kMerge = kWarps * G * 128 * 4;             // per-warp O
-  static constexpr uint32_t kML = kWarps * G * 2 * 4;
-  static constexpr uint32_t kBars = kWarps * kSlots * 8;
-  static constexpr size_t kTotal = 128 + kRing + kMerge + kML + kBars;
+enum {
+  B_Q = 0, B_FULL = 1, B_EMPTY = 1 + kStages, B_SFULL = 1 + 2 * kStages, B_SFREE = B_SFULL + 2,
+  B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_DRAIN = B_PVDONE + 2, B_COUNT = B_DRAIN + 1
 };
 
-__device__ __forceinline__ void unpack8(uint4 raw, float* f) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CC_R8(0), CC_R8(8)
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier over `threads` threads that also ANDs a predicate across them: the softmax warps
+// take every give-up decision together, so none waits at a barrier the others left.
+__device__ __forceinline__ bool bar_and(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// Page id of page index p of sequence row `pt`, or -1 when the entry lies outside the table
+// or names no page of the pool.
+__device__ __forceinline__ int page_id(const int32_t* pt, int p, int max_pages, int n_pages) {
+  if (p < 0 || p >= max_pages) return -1;
+  const int id = pt[p];
+  return (id >= 0 && id < n_pages) ? id : -1;
 }
 
 template <int G>
-__global__ void __launch_bounds__(kWarps * 32)
-    k_attn_decode(const __nv_bfloat16* __restrict__ q, int ld_q,
-                  const __nv_bfloat16* __restrict__ kpool, const __nv_bfloat16* __restrict__ vpool,
-                  int n_pages, const int32_t* __restrict__ page_table, int max_pages,
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_decode(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, int n_pages,
+                  const int32_t* __restrict__ page_table, int max_pages,
                   const int32_t* __restrict__ n_keys, int n_kv, int window, int splits,
                   float scale_log2, float* __restrict__ part_o, float* __restrict__ part_ml,
                   int* err) {
-  using L = DecSmem<G>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-  uint8_t* ring = smem;
-  float* wo = reinterpret_cast<float*>(smem + L::kRing);             // [warp][G][128]
-  float* wml = reinterpret_cast<float*>(smem + L::kRing + L::kMerge);  // [warp][G][2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kRing + L::kMerge + L::kML);
-
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int n_q = n_kv * G;
-  const int warp = warp_id(), lane = lane_id();
   const int n = n_keys[b];
   const int lo = window > 0 ? max(0, n - window) : 0;
-  const int p_first = lo / kPage, p_last = (n - 1) / kPage;
-  const int sp0 = p_first + split * kPagesPerSplit;
-  const int sp1 = min(p_last, sp0 + kPagesPerSplit - 1);
+  const int t_first = lo / kTileKeys, t_last = (n - 1) / kTileKeys;   // key tiles in view
+  const int st0 = t_first + split * kTilesPerSplit;
+  const int n_tiles = n <= 0 ? 0 : min(t_last, st0 + kTilesPerSplit - 1) - st0 + 1;
   const size_t part_base = ((size_t)b * n_q + (size_t)g * G) * splits + split;
-
-  if (n <= 0 || sp0 > sp1) {  // nothing to attend in this split
+  if (n_tiles <= 0) {  // nothing to attend in this split
     if (threadIdx.x < G) {
       part_ml[(part_base + (size_t)threadIdx.x * splits) * 2 + 0] = -INFINITY;
       part_ml[(part_base + (size_t)threadIdx.x * splits) * 2 + 1] = 0.f;
@@ -86,196 +144,245 @@ __global__ void __launch_bounds__(kWarps * 32)
     return;
   }
 
-  // pages of this warp: sp0 + warp + kWarps * i, i < cnt
-  const int cnt = (sp1 - sp0 - warp) >= 0 ? (sp1 - sp0 - warp) / kWarps + 1 : 0;
-  const uint32_t ring_w = smem_u32(ring) + warp * kSlots * kSlotBytes;
-  const uint32_t bar_w = smem_u32(bars) + warp * kSlots * 8;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
   const int32_t* pt = page_table + (size_t)b * max_pages;
 
-  // page id of this warp's i-th page; an id outside the pool is reported and replaced by
-  // page 0 (its keys are masked) so that the ring's phase accounting stays regular
-  auto page_of = [&](int i, bool* valid) -> int {
-    const int p = sp0 + warp + kWarps * i;
-    const int id = pt[p];
-    *valid = id >= 0 && id < n_pages;
-    return *valid ? id : 0;
-  };
-  int issued = 0;
-  auto issue = [&](int i) {
-    bool valid;
-    const int id = page_of(i, &valid);
-    if (!valid) set_error(err, CC_DEV_CHECK);
-    const int slot = i % kSlots;
-    const uint32_t bar = bar_w + 8 * slot;
-    const size_t off = ((size_t)id * n_kv + g) * (kPage * 128);
-    mbar_expect_tx(bar, kSlotBytes);
-    bulk_load(ring_w + slot * kSlotBytes, kpool + off, kPageBytes, bar);
-    bulk_load(ring_w + slot * kSlotBytes + kPageBytes, vpool + off, kPageBytes, bar);
-    ++issued;
-  };
-
-  if (lane == 0) {
-    for (int s = 0; s < kSlots; ++s) mbar_init(bar_w + 8 * s, 1);
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(bar(B_Q), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SFREE + i), 128);
+      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_PVDONE + i), 1);
+    }
+    mbar_init(bar(B_DRAIN), 1);
     fence_mbar_init();
   }
-  __syncwarp();
-  if (lane == 0) {
-    for (int i = 0; i < kSlots && i < cnt; ++i) issue(i);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
   }
+  // P rows G..15 are padding: zero them once in both buffers
+  for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kThreads) {
+    const uint32_t off = i * 16;
+    const int row = (off % kPBytes % 2048) / 128;   // 16 rows of 128 B per 2 KB box
+    if (row >= G) st_shared_v4(sbase + kOffP + off, 0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  // this lane's 16 dims: [8*(lane%8), +8) and [64 + 8*(lane%8), +8); its key in a step of 4
-  const int sub = lane & 7, kg = lane >> 3;
-  float qf[G][16];
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_expect_tx(bar(B_Q), kQBytes);
+      tma_load_2d(sbase + kOffQ, &tm_q, bar(B_Q), 0, b * n_q + g * G);
+      tma_load_2d(sbase + kOffQ + kQBytes / 2, &tm_q, bar(B_Q), 64, b * n_q + g * G);
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(bar(B_EMPTY + s), ((i / kStages) & 1) ^ 1, err)) break;
+        mbar_expect_tx(bar(B_FULL + s), 2 * kTile);
+        const int p0 = (st0 + i) * kPagesPerTile;
+#pragma unroll 1
+        for (int p = 0; p < kPagesPerTile; ++p) {
+          int id = page_id(pt, p0 + p, max_pages, n_pages);
+          if (id < 0) id = 0;   // keys of such a page are masked by the softmax warps
+          const int y = (id * n_kv + g) * kPage;
+          const uint32_t dk = sbase + kOffK + s * kTile + p * (kPage * 128);
+          const uint32_t dv = sbase + kOffV + s * kTile + p * (kPage * 128);
+          tma_load_2d(dk, &tm_k, bar(B_FULL + s), 0, y);
+          tma_load_2d(dk + kHalf, &tm_k, bar(B_FULL + s), 64, y);
+          tma_load_2d(dv, &tm_v, bar(B_FULL + s), 0, y);
+          tma_load_2d(dv + kHalf, &tm_v, bar(B_FULL + s), 64, y);
+        }
+        ++issued;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(B_Q), 0, err);
+      auto issue_s = [&](int i) -> bool {
+        const int s = i % kStages;
+        if (!mbar_wait(bar(B_FULL + s), (i / kStages) & 1, err)) return false;
+        tc_fence_after();
+        const uint32_t kb = sbase + kOffK + s * kTile;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const __nv_bfloat16* qp = q + (size_t)b * ld_q + (size_t)(g * G + h) * 128;
-    unpack8(*reinterpret_cast<const uint4*>(qp + 8 * sub), qf[h]);
-    unpack8(*reinterpret_cast<const uint4*>(qp + 64 + 8 * sub), qf[h] + 8);
-  }
-  float m[G], l[G], o[G][16];
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
+          tc_mma(tmem + 16 * (i & 1), desc_kmajor_sw128(kb + off),
+                 desc_kmajor_sw128(sbase + kOffQ + qoff), kIdescS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(B_SFULL + (i & 1)));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_tiles > 1) ok = issue_s(1);
+      for (int i = 0; i < n_tiles && ok; ++i) {
+        const int h = i & 1;
+        if (i + 2 < n_tiles) {   // score buffer h is free once the softmax has read tile i
+          if (!mbar_wait(bar(B_SFREE + h), (i >> 1) & 1, err)) break;
+          if (!(ok = issue_s(i + 2))) break;
+        }
+        if (!mbar_wait(bar(B_PFULL + h), (i >> 1) & 1, err)) break;
+        tc_fence_after();
+        const uint32_t vb = sbase + kOffV + (i % kStages) * kTile;
+        const uint32_t pb = sbase + kOffP + h * kPBytes;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
+        for (int kk = 0; kk < 8; ++kk) {   // 16 keys per MMA
+          tc_mma(tmem + 32, desc_mnmajor_sw128(vb + kk * 2048, kHalf),
+                 desc_kmajor_sw128(pb + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32), kIdescPV,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bar(B_EMPTY + (i % kStages)));
+        tc_commit(bar(B_PVDONE + h));
+      }
+      tc_commit(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, nullptr);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax, key per thread
+    const int quarter = warp & 3;
+    const int t = quarter * 32 + lane;                  // key of the tile, TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float m[G], lsum[G];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
-  }
-
-  bool ok = true;
-  for (int i = 0; i < cnt && ok; ++i) {
-    const int slot = i % kSlots;
-    const int page_pos = sp0 + warp + kWarps * i;  // page index within the sequence
-    bool valid;
-    page_of(i, &valid);
-    {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_w + 8 * slot, (i / kSlots) & 1, err));
-      if (!ok) break;
-      const uint32_t ks = ring_w + slot * kSlotBytes;
-      const uint32_t vs = ks + kPageBytes;
-      float sc[4][G];
+    for (int hh = 0; hh < G; ++hh) {
+      m[hh] = -INFINITY;
+      lsum[hh] = 0.f;
+    }
+    bool ok = true;
+    int last = -1;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int h = i & 1;
+      if (!bar_and(2, 128, mbar_wait(bar(B_SFULL + h), (i >> 1) & 1, err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[16];
+      tmem_ld16(tmem + 16 * h + lane_off, s);
+      tc_fence_before();
+      mbar_arrive(bar(B_SFREE + h));
+      const int kj = (st0 + i) * kTileKeys + t;
+      bool vis = kj >= lo && kj < n;
+      if (vis && page_id(pt, kj / kPage, max_pages, n_pages) < 0) {
+        set_error(err, CC_DEV_CHECK);
+        vis = false;
+      }
+      // per-head maximum of the tile: warp shuffles, then the four warps via shared memory
+      float* rb = red + h * 64;
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const int key = st * 4 + kg;
-        uint4 r0, r1;
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0.x), "=r"(r0.y), "=r"(r0.z), "=r"(r0.w)
-                     : "r"(ks + key * 256 + sub * 16));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r1.x), "=r"(r1.y), "=r"(r1.z), "=r"(r1.w)
-                     : "r"(ks + key * 256 + 128 + sub * 16));
-        float kf[16];
-        unpack8(r0, kf);
-        unpack8(r1, kf + 8);
+      for (int hh = 0; hh < G; ++hh) {
+        s[hh] = vis ? s[hh] * scale_log2 : -INFINITY;
+        float x = s[hh];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float d = 0.f;
+        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if (lane == 0) rb[quarter * 16 + hh] = x;
+      }
+      named_barrier_sync(1, 128);
+      bool need_o = false;
+      float f[G];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) d = fmaf(qf[h][e], kf[e], d);
-          d += __shfl_xor_sync(0xffffffffu, d, 1);
-          d += __shfl_xor_sync(0xffffffffu, d, 2);
-          d += __shfl_xor_sync(0xffffffffu, d, 4);
-          const int kj = page_pos * kPage + key;
-          sc[st][h] = (valid && kj >= lo && kj < n) ? d * scale_log2 : -INFINITY;
+      for (int hh = 0; hh < G; ++hh) {
+        const float mt = fmaxf(fmaxf(rb[hh], rb[16 + hh]), fmaxf(rb[32 + hh], rb[48 + hh]));
+        f[hh] = 1.f;
+        if (mt > m[hh] + kRescaleThreshold) {   // uniform across the CTA
+          if (m[hh] != -INFINITY) {
+            f[hh] = ex2f(m[hh] - mt);
+            need_o = true;
+          }
+          m[hh] = mt;
         }
       }
+      if (need_o) {
+        // O^T holds the P V of earlier tiles: wait for the last one, rescale in TMEM
+        if (!bar_and(2, 128, mbar_wait(bar(B_PVDONE + (h ^ 1)), ((i - 1) >> 1) & 1, err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float o[16];
+        tmem_ld16(tmem + 32 + lane_off, o);
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float pm = fmaxf(fmaxf(sc[0][h], sc[1][h]), fmaxf(sc[2][h], sc[3][h]));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 8));
-        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-        const float mn = fmaxf(m[h], pm);
-        const float f = (m[h] == -INFINITY) ? 0.f : exp2f(m[h] - mn);
-        const float mu = (mn == -INFINITY) ? 0.f : mn;
-        l[h] *= f;
+        for (int hh = 0; hh < G; ++hh) o[hh] *= f[hh];
+        tmem_st16(tmem + 32 + lane_off, o);
+        tmem_st_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) o[h][e] *= f;
-        m[h] = mn;
-#pragma unroll
-        for (int st = 0; st < 4; ++st) sc[st][h] = exp2f(sc[st][h] - mu);
+        for (int hh = 0; hh < G; ++hh) lsum[hh] *= f[hh];
       }
+      // P buffer h was read by PV(i-2)
+      if (i >= 2 && !bar_and(2, 128, mbar_wait(bar(B_PVDONE + h), ((i - 2) >> 1) & 1, err))) {
+        ok = false;
+        break;
+      }
+      // P[hh][t] (row hh, key t) in the 128-byte-swizzled [16 x 128] bf16 buffer
+      const uint32_t pb = sbase + kOffP + h * kPBytes + (t >> 6) * (kPBytes / 2);
+      const int ch = (t & 63) >> 3;
 #pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const int key = st * 4 + kg;
-        uint4 r0, r1;
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0.x), "=r"(r0.y), "=r"(r0.z), "=r"(r0.w)
-                     : "r"(vs + key * 256 + sub * 16));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r1.x), "=r"(r1.y), "=r"(r1.z), "=r"(r1.w)
-                     : "r"(vs + key * 256 + 128 + sub * 16));
-        float vf[16];
-        unpack8(r0, vf);
-        unpack8(r1, vf + 8);
+      for (int hh = 0; hh < G; ++hh) {
+        const float p = ex2f(s[hh] - (m[hh] == -INFINITY ? 0.f : m[hh]));
+        lsum[hh] += p;
+        const uint32_t addr = pb + hh * 128 + ((ch ^ (hh & 7)) << 4) + ((t & 7) << 1);
+        const __nv_bfloat16 pv = __float2bfloat16_rn(p);
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&pv))
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + h));
+      last = i;
+    }
+    if (ok && last >= 0)
+      ok = bar_and(2, 128, mbar_wait(bar(B_PVDONE + (last & 1)), (last >> 1) & 1, err));
+    // sum the per-key partial sums over the 128 threads
+    named_barrier_sync(1, 128);
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float p = sc[st][h];
-          l[h] += p;
+    for (int hh = 0; hh < G; ++hh) {
+      float x = lsum[hh];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[h][e] = fmaf(p, vf[e], o[h][e]);
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0) red[quarter * 16 + hh] = x;
+    }
+    named_barrier_sync(1, 128);
+    tc_fence_after();
+    if (ok) {
+      float o[16];
+      tmem_ld16(tmem + 32 + lane_off, o);   // lane t holds dim t of every head
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const size_t pb2 = part_base + (size_t)hh * splits;
+        part_o[pb2 * 128 + t] = o[hh];
+        if (t == 0) {
+          part_ml[pb2 * 2 + 0] = m[hh];
+          part_ml[pb2 * 2 + 1] = red[hh] + red[16 + hh] + red[32 + hh] + red[48 + hh];
         }
       }
     }
-    __syncwarp();
-    if (lane == 0 && i + kSlots < cnt) issue(i + kSlots);
-  }
-
-  // the four key groups of the warp hold disjoint keys: sum them
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
-    l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], 8);
-      o[h][e] += __shfl_xor_sync(0xffffffffu, o[h][e], 16);
-    }
-  }
-  if (lane < 8) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float* dst = wo + ((size_t)warp * G + h) * 128;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        dst[8 * sub + e] = o[h][e];
-        dst[64 + 8 * sub + e] = o[h][8 + e];
-      }
-    }
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      wml[(warp * G + h) * 2 + 0] = m[h];
-      wml[(warp * G + h) * 2 + 1] = l[h];
-    }
-  }
-  // drain: a slot issued but not consumed (only after a failed wait) must land first
-  if (lane == 0 && !ok) {
-    for (int i = max(0, issued - kSlots); i < issued; ++i)
-      mbar_wait(bar_w + 8 * (i % kSlots), (i / kSlots) & 1, nullptr);
   }
   __syncthreads();
-  // merge the warps: thread t owns dim t of every head
-  const int d = threadIdx.x;
-#pragma unroll 1
-  for (int h = 0; h < G; ++h) {
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * G + h) * 2]);
-    float O = 0.f, Lsum = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = wml[(w * G + h) * 2];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
-        O += f * wo[((size_t)w * G + h) * 128 + d];
-        Lsum += f * wml[(w * G + h) * 2 + 1];
-      }
-    }
-    const size_t pb = part_base + (size_t)h * splits;
-    part_o[pb * 128 + d] = O;
-    if (d == 0) {
-      part_ml[pb * 2 + 0] = M;
-      part_ml[pb * 2 + 1] = Lsum;
-    }
+  if (warp == 0 && lane == 0) {
+    // a failed launch may leave loads in flight: let them land (bounded)
+    for (int i = max(0, issued - kStages); i < issued; ++i)
+      mbar_wait(bar(B_FULL + (i % kStages)), (i / kStages) & 1, nullptr);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -299,23 +406,22 @@ __global__ void __launch_bounds__(128)
   out[(size_t)b * ld_out + (size_t)h * 128 + d] = __float2bfloat16_rn(Lsum > 0.f ? O / Lsum : 0.f);
 }
 
+
 template <int G>
-cc_status launch_dec(const __nv_bfloat16* q, int ld_q, const __nv_bfloat16* kp,
-                     const __nv_bfloat16* vp, int n_pages, const int32_t* pt, int max_pages,
-                     const int32_t* n_keys, int batch, int n_kv, int window, int splits,
-                     DecodeScratch scr, int* err, cudaStream_t s) {
-  using L = DecSmem<G>;
+cc_status launch_dec(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     int n_pages, const int32_t* pt, int max_pages, const int32_t* n_keys,
+                     int batch, int n_kv, int window, int splits, DecodeScratch scr, int* err,
+                     cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     CC_CHECK_CUDA(cudaFuncSetAttribute(k_attn_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(L::kTotal)));
+                                       static_cast<int>(kSmem)));
     attr_set = true;
   }
   const float sl2 = (1.0f / sqrtf(128.0f)) * kLog2e;
   dim3 grid(splits, n_kv, batch);
-  k_attn_decode<G><<<grid, kWarps * 32, L::kTotal, s>>>(q, ld_q, kp, vp, n_pages, pt, max_pages,
-                                                        n_keys, n_kv, window, splits, sl2,
-                                                        scr.part_o, scr.part_ml, err);
+  k_attn_decode<G><<<grid, kThreads, kSmem, s>>>(tq, tk, tv, n_pages, pt, max_pages, n_keys, n_kv,
+                                                 window, splits, sl2, scr.part_o, scr.part_ml, err);
   CC_CHECK_CUDA(cudaGetLastError());
   return CC_OK;
 }
@@ -334,19 +440,27 @@ cc_status launch_attn_decode(const __nv_bfloat16* q, int ld_q, const __nv_bfloat
                              int page_size, int window, DecodeScratch scr, __nv_bfloat16* out,
                              int ld_out, int* err, cudaStream_t s) {
   if (batch <= 0) return CC_OK;
-  if (page_size != kPage || n_q % n_kv != 0) return CC_ERR_UNSUPPORTED;
-  const int splits = decode_splits(max_pages);
+  if (page_size != kPage || n_q % n_kv != 0 || ld_q != n_q * 128) return CC_ERR_UNSUPPORTED;
   const int G = n_q / n_kv;
+  CUtensorMap tq, tk, tv;
+  const uint64_t pool_rows = (uint64_t)n_pages * n_kv * kPage;
+  if (!make_tmap_bf16_2d(&tq, q, (uint64_t)batch * n_q, 128, 128, kQRows, 64) ||
+      !make_tmap_bf16_2d(&tk, k_pool, pool_rows, 128, 128, kPage, 64) ||
+      !make_tmap_bf16_2d(&tv, v_pool, pool_rows, 128, 128, kPage, 64))
+    return CC_ERR_INVALID_ARG;
+  const int splits = decode_splits(max_pages);
   cc_status st;
   switch (G) {
-    case 1: st = launch_dec<1>(q, ld_q, k_pool, v_pool, n_pages, page_table, max_pages, n_keys,
-                               batch, n_kv, window, splits, scr, err, s); break;
-    case 2: st = launch_dec<2>(q, ld_q, k_pool, v_pool, n_pages, page_table, max_pages, n_keys,
-                               batch, n_kv, window, splits, scr, err, s); break;
-    case 4: st = launch_dec<4>(q, ld_q, k_pool, v_pool, n_pages, page_table, max_pages, n_keys,
-                               batch, n_kv, window, splits, scr, err, s); break;
-    case 8: st = launch_dec<8>(q, ld_q, k_pool, v_pool, n_pages, page_table, max_pages, n_keys,
-                               batch, n_kv, window, splits, scr, err, s); break;
+    case 1: st = launch_dec<1>(tq, tk, tv, n_pages, page_table, max_pages, n_keys, batch, n_kv,
+                               window, splits, scr, err, s); break;
+    case 2: st = launch_dec<2>(tq, tk, tv, n_pages, page_table, max_pages, n_keys, batch, n_kv,
+                               window, splits, scr, err, s); break;
+    case 4: st = launch_dec<4>(tq, tk, tv, n_pages, page_table, max_pages, n_keys, batch, n_kv,
+                               window, splits, scr, err, s); break;
+    case 8: st = launch_dec<8>(tq, tk, tv, n_pages, page_table, max_pages, n_keys, batch, n_kv,
+                               window, splits, scr, err, s); break;
+    case 16: st = launch_dec<16>(tq, tk, tv, n_pages, page_table, max_pages, n_keys, batch, n_kv,
+                                 window, splits, scr, err, s); break;
     default: return CC_ERR_UNSUPPORTED;
   }
   if (st != CC_OK) return st;

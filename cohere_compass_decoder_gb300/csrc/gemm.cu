@@ -367,17 +367,22 @@ cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
 
 }  // namespace
 
+// Tile shape and K splitting. With one row tile (M <= 128: decode steps, the head on a few
+// rows) the GEMM streams its weights from HBM, so the choice maximises the number of CTAs
+// reading them: 128-wide tiles and, for additive epilogues, K splits up to one CTA per SM.
+// With several row tiles it is tensor bound and the 128 x 256 tile (the one whose operand
+// traffic fits shared-memory bandwidth best) is kept unless it leaves most SMs idle.
 void gemm_choose(int M, int N, int K, int epi, int* bn, int* splits) {
   const int sms = num_sms();
   const int m_tiles = (M + kBM - 1) / kBM;
   const int kbt = K / kBK;
   int b = (N % 256 == 0) ? 256 : 128;
-  // small M (decode, the head on a few rows): narrower tiles give every SM a weight slice
-  if (b == 256 && m_tiles * (N / 256) < sms) b = 128;
+  if (b == 256 && m_tiles * (N / 256) * 2 < sms) b = 128;
+  if (b == 256 && m_tiles == 1 && (N / 256) < sms) b = 128;
   int sp = 1;
   const bool additive = (epi == EPI_RESID) || (epi == EPI_F32);
-  if (additive) {
-    const int units = m_tiles * (N / b);
+  if (additive && m_tiles == 1) {
+    const int units = N / b;
     while (units * (sp + 1) <= sms && kbt / (sp + 1) >= 4) ++sp;
   }
   *bn = b;

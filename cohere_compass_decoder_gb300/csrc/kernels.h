@@ -61,9 +61,11 @@ struct AttnTile {
 };
 
 // Builds the list of 128-query tiles of all sequences, heaviest first.
-cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int window, AttnTile* tiles,
-                            int32_t* n_tiles, cudaStream_t s);
+cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int window,
+                            AttnTile* tiles, int32_t* n_tiles, cudaStream_t s);
 int attn_max_tiles(int tokens, int n_seqs);
+// Rows (keys) of the K and V boxes the prefill attention kernel loads.
+int attn_kv_box_rows();
 
 cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               __nv_bfloat16* out, int ld_out, const AttnTile* tiles,

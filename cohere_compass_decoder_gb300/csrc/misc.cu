@@ -1,4 +1,6 @@
 // Memory-bound helpers of the path: LayerNorm, the MRoPE cos/sin table, row maps.
+#include <cmath>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -91,9 +93,14 @@ cc_status launch_ln(const float* x, const void* gamma, OutT* out, int rows, int 
 // ---------------------------------------------------------------------- MRoPE table
 // mlxcel issue "Text decoder forward", interleaved MRoPE: frequency j (< d/2) reads the h
 // axis when j % 3 == 1 and j < 3 s_h, the w axis when j % 3 == 2 and j < 3 s_w, else t;
-// angle = pos[axis] * theta^(-2j/d). The angle (up to ~1e5 rad) is formed and reduced
-// modulo 2*pi in double precision; sincosf then sees |r| <= pi.
-__global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, double theta,
+// angle = pos[axis] * theta^(-2j/d). theta^(-2j/d) is evaluated once per call on the host
+// in double precision; the angle (up to ~1e5 rad) is formed and reduced modulo 2*pi in
+// double precision; sincosf then sees |r| <= pi.
+struct InvFreq {
+  double v[64];
+};
+
+__global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, const InvFreq f,
                               int sec_h, int sec_w, float2* __restrict__ table) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= T * half) return;
@@ -101,10 +108,10 @@ __global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, 
   int axis = 0;
   if (j % 3 == 1 && j < 3 * sec_h) axis = 1;
   else if (j % 3 == 2 && j < 3 * sec_w) axis = 2;
-  const double inv_freq = pow(theta, -2.0 * j / (2.0 * half));
-  const double ang = static_cast<double>(pos[axis * T + t]) * inv_freq;
+  const double ang = static_cast<double>(pos[axis * T + t]) * f.v[j];
   const double two_pi = 6.283185307179586476925286766559;
-  const double r = ang - two_pi * rint(ang / two_pi);
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  const double r = fma(-two_pi, rint(ang * inv_two_pi), ang);
   float sn, cs;
   sincosf(static_cast<float>(r), &sn, &cs);
   table[idx] = make_float2(cs, sn);
@@ -184,9 +191,11 @@ cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double the
                              const int32_t section[3], float2* table, cudaStream_t s) {
   if (T <= 0) return CC_OK;
   const int half = head_dim / 2;
+  if (half > 64) return CC_ERR_UNSUPPORTED;
+  InvFreq f{};
+  for (int j = 0; j < half; ++j) f.v[j] = std::pow(theta, -2.0 * j / head_dim);
   const int n = T * half;
-  k_mrope_table<<<(n + 255) / 256, 256, 0, s>>>(pos, T, half, theta, section[1], section[2],
-                                                table);
+  k_mrope_table<<<(n + 255) / 256, 256, 0, s>>>(pos, T, half, f, section[1], section[2], table);
   CC_CHECK_CUDA(cudaGetLastError());
   return CC_OK;
 }

@@ -55,9 +55,10 @@ typedef enum { CC_F32 = 0, CC_BF16 = 1 } cc_dtype;
  * num_layers entries of cc_layer_type and is copied by cc_layer_plan_create.
  * Requirements (else CC_ERR_INVALID_ARG): mrope_section sums to head_dim/2;
  * n_q_heads % n_kv_heads == 0; sliding_window > 0; all sizes > 0.
- * bf16 plans also need (else CC_ERR_UNSUPPORTED): head_dim == 128; hidden_size and
- * intermediate_size multiples of 128; (n_q + 2*n_kv)*head_dim a multiple of 256;
- * vocab_size a multiple of 128. f32 plans need head_dim <= 128 and even. */
+ * All plans need hidden_size a multiple of 128 and at most 4096, intermediate_size a
+ * multiple of 64 (else CC_ERR_UNSUPPORTED). bf16 plans also need head_dim == 128,
+ * vocab_size a multiple of 128, kv_page_size == 16 and n_q / n_kv one of 1, 2, 4, 8, 16.
+ * f32 plans need head_dim <= 128. */
 typedef struct {
   int32_t num_layers;
   int32_t hidden_size;
@@ -80,7 +81,7 @@ typedef struct {
 /* One layer's weights, packed by cc_pack_layer_weights:
  *  ln_w [H]                    LayerNorm gain
  *  w1   [N1, H], N1 = (n_q + 2 n_kv) d + 2 I: rows q | k | v | then the SwiGLU gate and
- *       up rows interleaved in blocks of 128 (gate 0..127, up 0..127, gate 128..255, ...)
+ *       up rows interleaved in blocks of 64 (gate 0..63, up 0..63, gate 64..127, ...)
  *  w2   [H, K2], K2 = n_q d + I: columns o_proj | down_proj
  * The plan borrows these pointers; they must outlive it. */
 typedef struct {
@@ -260,7 +261,7 @@ cc_status cc_op_attention_prefill(const void* q, const void* k, const void* v, v
  * CC_ERR_DEVICE_CHECK and their keys are skipped); n_keys int32 [batch] keys to attend
  * over (token n_keys-1 is the query's own, n_keys <= max_pages * page_size);
  * window > 0: only the last `window` keys; out bf16 rows of leading dimension ld_out.
- * page_size must be 16 and n_q / n_kv one of 1, 2, 4, 8 (else CC_ERR_UNSUPPORTED). */
+ * page_size must be 16 and n_q / n_kv one of 1, 2, 4, 8, 16 (else CC_ERR_UNSUPPORTED). */
 cc_status cc_op_attention_decode(const void* q, const void* k_pool, const void* v_pool,
                                  int32_t n_pages, const int32_t* page_table, int32_t max_pages,
                                  const int32_t* n_keys, int32_t batch, int32_t n_q,
@@ -278,7 +279,7 @@ cc_status cc_op_sync(void* stream);
  * may impose, or a host that is not allowed to allocate at all.
  * Same inputs, outputs and result as cc_op_attention_decode. Its split-KV scratch is one
  * fixed array inside the library (16 MiB, held on every GPU that loads the library until
- * the process exits): it needs batch * n_q * ceil(max_pages / 16) * 130 floats, at most
+ * the process exits): it needs batch * n_q * ceil(max_pages / 64) * 130 floats, at most
  * 4194304; larger problems return CC_ERR_INVALID_ARG and launch nothing.
  * The first call on a device looks up that array's device address (with that device
  * current) and caches it; make that first call before any stream capture. All calls share

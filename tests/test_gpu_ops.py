@@ -91,12 +91,19 @@ def test_gemm_accumulates():
 
 
 # --------------------------------------------------------------------------- prefill attention
-def _attn_case(lens, nq, nkv, window, seed):
+def _attn_case(lens, nq, nkv, window, seed, qscale=1.0, ramp=0.0):
+    """ramp > 0 adds a score bias growing with the key index (so the running max keeps
+    moving and the output rescaling runs): k[j] += ramp * j / T * u with q . u > 0."""
     rng = np.random.default_rng(seed)
     T = sum(lens)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
-    q = bf16_dev(rng.standard_normal((T, nq * 128)))
-    k = bf16_dev(rng.standard_normal((T, nkv * 128)))
+    qn = rng.standard_normal((T, nq * 128)) * qscale
+    kn = rng.standard_normal((T, nkv * 128))
+    if ramp:
+        qn[:, ::128] = np.abs(qn[:, ::128]) + 1.0
+        kn[:, ::128] += ramp * np.arange(T)[:, None] / T
+    q = bf16_dev(qn)
+    k = bf16_dev(kn)
     v = bf16_dev(rng.standard_normal((T, nkv * 128)))
     ld = nq * 128 + 64
     out = torch.full((T, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -124,6 +131,14 @@ def test_attention_prefill_matches_oracle(lens, nq, nkv, window):
     assert_close(got, want, 2e-2, 2e-3, "attention")
 
 
+@pytest.mark.parametrize("lens,window,qscale,ramp", [
+    ([700], 0, 4.0, 0.0), ([700], 300, 4.0, 0.0), ([900], 0, 1.0, 300.0), ([513, 400], 0, 2.0, 200.0),
+])
+def test_attention_prefill_large_scores(lens, window, qscale, ramp):
+    got, want = _attn_case(lens, 4, 2, window, seed=77 + len(lens), qscale=qscale, ramp=ramp)
+    assert_close(got, want, 2e-2, 2e-3, "attention (large scores)")
+
+
 def test_attention_window_at_least_sequence_equals_full():
     rng = np.random.default_rng(5)
     T, nq, nkv = 333, 4, 2
@@ -139,11 +154,12 @@ def test_attention_window_at_least_sequence_equals_full():
 
 
 # --------------------------------------------------------------------------- decode attention
-@pytest.mark.parametrize("nq,nkv,window", [(8, 2, 0), (8, 2, 200), (16, 4, 0), (4, 4, 37),
-                                           (8, 1, 0)])
-def test_attention_decode_matches_oracle(nq, nkv, window):
-    rng = np.random.default_rng(nq * 13 + nkv + window)
-    B, ps, max_pages = 7, 16, 44
+@pytest.mark.parametrize("nq,nkv,window,max_pages", [
+    (8, 2, 0, 44), (8, 2, 200, 44), (16, 4, 0, 44), (4, 4, 37, 44), (8, 1, 0, 44),
+    (16, 1, 0, 44), (16, 4, 0, 300), (16, 4, 1500, 300)])
+def test_attention_decode_matches_oracle(nq, nkv, window, max_pages):
+    rng = np.random.default_rng(nq * 13 + nkv + window + max_pages)
+    B, ps = 7, 16
     n_pages = B * max_pages + 5
     n_keys = rng.integers(1, max_pages * ps + 1, size=B).astype(np.int32)
     n_keys[0] = 1

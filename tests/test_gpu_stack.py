@@ -159,11 +159,75 @@ def test_decode_continues_prefill_on_gpu():
     assert mx <= TOL_MAX and mn <= TOL_MEAN, (mx, mn)
 
 
-@pytest.mark.slow
-def test_cfg3_stack28():
+@pytest.fixture(scope="module")
+def cfg3_oracle():
+    """The 28-layer workload's inputs and the oracle's residual stream after every layer."""
+    from oracle import decoder as O
     inp = Inputs(cfg3())
+    wl = inp.wl
+    pos, _ = O.positions(wl.seq_lens, [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w)
+                                       for i in wl.images])
+    ds = [inp.ds(i) for i in range(wl.n_deepstack)]
+    h, hs = O.prefill(inp.hidden, inp.layer, O.shape_dict(inp.shape), pos, inp.cu_seqlens,
+                      inp.ds_rows, ds, True, return_all=True)
+    lg = O.logits(h[inp.head_rows], inp.final_ln, inp.embed, O.shape_dict(inp.shape), True)
+    return inp, hs, lg
+
+
+class _OneLayer(Inputs):
+    """Layer i of the 28-layer workload alone, fed with a given residual stream."""
+
+    def __init__(self, base, i, hidden):
+        import dataclasses
+        shape = dataclasses.replace(base.shape, num_layers=1,
+                                    layer_types=(base.shape.layer_types[i],), vocab_size=128)
+        n_ds = 1 if i < base.wl.n_deepstack else 0
+        super().__init__(dataclasses.replace(base.wl, shape=shape, n_deepstack=n_ds))
+        self.base, self.i = base, i
+        self._misc = dict(hidden=hidden.astype(np.float32), final_ln=base.final_ln)
+        self._ds["embed"] = np.zeros((128, shape.hidden_size), np.uint16)
+
+    def layer(self, j):
+        return self.base.layer(self.i)
+
+    def ds(self, j):
+        return self.base.ds(self.i)
+
+
+@pytest.mark.slow
+def test_cfg3_every_layer_from_oracle_input(cfg3_oracle):
+    """Each of the 28 layers (with its deepstack add) on the GPU, started from the oracle's
+    residual stream before it, matches the oracle's stream after it within the stack
+    tolerance (2e-2 max-abs, 2e-3 mean-abs)."""
+    inp, hs, _ = cfg3_oracle
+    prev = inp.hidden.astype(np.float64)
+    worst = []
+    for i in range(inp.shape.num_layers):
+        one = _OneLayer(inp, i, prev)
+        gw = GpuWorkload(one)
+        h = gw.fresh_hidden()
+        gw.prefill(h)
+        gw.sync()
+        mx, mn = assert_close(as_numpy(h), hs[i], TOL_MAX, TOL_MEAN, f"layer {i}")
+        worst.append((mx, mn))
+        gw.close()
+        prev = hs[i]
+    print("per-layer max/mean:", worst)
+
+
+@pytest.mark.slow
+def test_cfg3_stack28(cfg3_oracle):
+    """The whole 28-layer stack and the head, end to end. Two bf16 implementations that
+    round the same intermediates drift apart by independent rounding noise once any
+    residual differs by an ulp; the oracle's own bf16-mirror mode drifts from its exact fp64
+    mode by 0.040 mean-abs / 0.24 max-abs after these 28 layers (per-layer growth about
+    1.4e-3). The end-to-end bound is therefore 1.5x that floor: 0.06 mean-abs, 0.5 max-abs
+    on the final hidden state; the logits keep the stack tolerance."""
+    inp, hs, lg_ref = cfg3_oracle
     gw, h, lg = _run(inp)
-    _check(inp, gw, h, lg)
+    assert_close(as_numpy(h), hs[-1], 0.5, 0.06, "hidden after 28 layers")
+    lmx, _ = assert_close(as_numpy(lg), lg_ref, TOL_MAX, TOL_MEAN, "logits")
+    assert lmx / np.abs(lg_ref).max() <= 0.1
 
 
 @pytest.mark.slow
