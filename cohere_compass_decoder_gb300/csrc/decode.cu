@@ -8,19 +8,20 @@
 // library's: pool [page][kv_head][16 tokens][128], so one page of one KV head is a 4 KB
 // contiguous block.
 //
-// Kernel 1, one CTA per (key split, KV head, sequence), 6 warps:
-//   warp 0      TMA: the G query heads of the KV head (one 16-row box), then per tile of 128
-//               keys the 8 pages of K and of V, gathered through the page table straight
-//               into 128-byte-swizzled tiles (3-stage ring)
-//   warp 1      MMA: S^T = K Q^T (M = 128 keys, N = 16 query rows of which G are used) into
-//               one of two TMEM score buffers, then O^T += V^T P (V read MN-major as the A
-//               operand, P = [16 x 128 keys] bf16 in shared memory)
-//   warps 2..5  softmax, one key per thread: masked scores of its G heads from TMEM, the
-//               tile's per-head maximum through shuffles and shared memory, the running
-//               maximum moved (and O^T rescaled in TMEM) only when it grows by more than 2^8,
-//               p = 2^(s - m), per-thread partial sums, P into shared memory.
-// Each K/V byte is read from HBM once for all G query heads and every multiply runs on the
-// tensor cores, so the kernel streams HBM instead of issuing CUDA-core FMAs.
+// Kernel 1, one CTA per (split of up to 1024 keys, KV head, sequence), 6 warps, two passes:
+//   warp 0      TMA: the G query heads of the KV head (one 16-row box), then the split's K
+//               tiles and after them its V tiles (128 keys each: the 8 pages gathered
+//               through the page table straight into 128-byte-swizzled tiles) through one
+//               2-stage ring
+//   warp 1      MMA: S^T_i = K_i Q^T for every tile i (M = 128 keys, N = 16 query rows of
+//               which G are used) into its own 16 TMEM columns; then O^T += V_i^T P_i (V read
+//               MN-major as the A operand, P_i = [16 x 128 keys] bf16 in shared memory)
+//   warps 2..5  softmax, one key of every tile per thread: the split's per-head maximum
+//               (shuffles, then the four warps through shared memory), p = 2^(s - max),
+//               P tiles into shared memory, per-head sums.
+// With one maximum per split there is no rescaling, and the CTA synchronises twice in all.
+// Each K/V byte is read from HBM once for all G query heads; the CTA needs about 100 KB of
+// shared memory, so two CTAs share an SM and cover each other's latencies.
 // Kernel 2 merges the splits of each (sequence, head) and writes O as bf16.
 #include <mutex>
 
@@ -37,28 +38,27 @@ constexpr int kTileKeys = 128;
 constexpr int kPagesPerTile = kTileKeys / kPage;   // 8
 constexpr int kTilesPerSplit = 8;                  // 1024 keys per CTA
 constexpr int kPagesPerSplit = kPagesPerTile * kTilesPerSplit;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 constexpr int kQRows = 16;                         // MMA N (query heads, padded)
 constexpr uint32_t kTile = kTileKeys * 128 * 2;    // 32 KB: 128 keys x 128 dims
 constexpr uint32_t kHalf = kTileKeys * 64 * 2;     // one 64-dim box column: 16 KB
 constexpr uint32_t kQBytes = kQRows * 128 * 2;     // 4 KB
-constexpr uint32_t kPBytes = kQRows * kTileKeys * 2;   // 4 KB
+constexpr uint32_t kPBytes = kQRows * kTileKeys * 2;   // 4 KB per tile
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = 4096;                   // 1024-aligned
-constexpr uint32_t kOffV = kOffK + kStages * kTile;
-constexpr uint32_t kOffP = kOffV + kStages * kTile;
-constexpr uint32_t kOffRed = kOffP + 2 * kPBytes;  // [2][4 warps][16] floats
-constexpr uint32_t kOffBar = kOffRed + 2 * 4 * 16 * 4;
+constexpr uint32_t kOffRing = 4096;                // 1024-aligned
+constexpr uint32_t kOffP = kOffRing + kStages * kTile;
+constexpr uint32_t kOffRed = kOffP + kTilesPerSplit * kPBytes;   // [4 warps][16] floats
+constexpr uint32_t kOffBar = kOffRed + 4 * 16 * 4;
 constexpr size_t kSmem = 1024 + kOffBar + 256;
-constexpr uint32_t kTmemCols = 64;                 // S0 | S1 | O (16 columns each)
+constexpr uint32_t kTmemCols = 256;                // S^T of 8 tiles (16 columns each) | O^T
+constexpr uint32_t kTmemO = 16 * kTilesPerSplit;
 constexpr uint32_t kIdescS = idesc_bf16(128, kQRows, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, kQRows, 0) | (1u << 15);   // A MN-major
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleThreshold = 8.0f;
 
 enum {
-  B_Q = 0, B_FULL = 1, B_EMPTY = 1 + kStages, B_SFULL = 1 + 2 * kStages, B_SFREE = B_SFULL + 2,
-  B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 2, B_DRAIN = B_PVDONE + 2, B_COUNT = B_DRAIN + 1
+  B_Q = 0, B_FULL = 1, B_EMPTY = 1 + kStages, B_SFULL = 1 + 2 * kStages, B_PFULL = B_SFULL + 1,
+  B_ODONE = B_PFULL + 1, B_DRAIN = B_ODONE + 1, B_COUNT = B_DRAIN + 1
 };
 
 __device__ __forceinline__ float ex2f(float x) {
@@ -78,19 +78,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
@@ -121,7 +108,7 @@ __device__ __forceinline__ int page_id(const int32_t* pt, int p, int max_pages, 
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_attn_decode(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, int n_pages,
                   const int32_t* __restrict__ page_table, int max_pages,
@@ -134,9 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lo = window > 0 ? max(0, n - window) : 0;
   const int t_first = lo / kTileKeys, t_last = (n - 1) / kTileKeys;   // key tiles in view
   const int st0 = t_first + split * kTilesPerSplit;
-  const int n_tiles = n <= 0 ? 0 : min(t_last, st0 + kTilesPerSplit - 1) - st0 + 1;
+  const int nt = n <= 0 ? 0 : min(t_last, st0 + kTilesPerSplit - 1) - st0 + 1;
   const size_t part_base = ((size_t)b * n_q + (size_t)g * G) * splits + split;
-  if (n_tiles <= 0) {  // nothing to attend in this split
+  if (nt <= 0) {  // nothing to attend in this split
     if (threadIdx.x < G) {
       part_ml[(part_base + (size_t)threadIdx.x * splits) * 2 + 0] = -INFINITY;
       part_ml[(part_base + (size_t)threadIdx.x * splits) * 2 + 1] = 0.f;
@@ -160,12 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 128);
-      mbar_init(bar(B_PFULL + i), 128);
-      mbar_init(bar(B_PVDONE + i), 1);
-    }
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_PFULL), 128);
+    mbar_init(bar(B_ODONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     fence_mbar_init();
   }
@@ -173,11 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-  // P rows G..15 are padding: zero them once in both buffers
-  for (int i = threadIdx.x; i < 2 * kPBytes / 16; i += kThreads) {
-    const uint32_t off = i * 16;
-    const int row = (off % kPBytes % 2048) / 128;   // 16 rows of 128 B per 2 KB box
-    if (row >= G) st_shared_v4(sbase + kOffP + off, 0u, 0u, 0u, 0u);
+  // P rows G..15 are padding: zero them in every tile buffer
+  if (G < kQRows) {
+    for (int i = threadIdx.x; i < kTilesPerSplit * kPBytes / 16; i += kThreads) {
+      const uint32_t off = i * 16;
+      const int row = (off % 2048) / 128;   // 16 rows of 128 B per 2 KB box
+      if (row >= G) st_shared_v4(sbase + kOffP + off, 0u, 0u, 0u, 0u);
+    }
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -191,22 +177,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(bar(B_Q), kQBytes);
       tma_load_2d(sbase + kOffQ, &tm_q, bar(B_Q), 0, b * n_q + g * G);
       tma_load_2d(sbase + kOffQ + kQBytes / 2, &tm_q, bar(B_Q), 64, b * n_q + g * G);
-      for (int i = 0; i < n_tiles; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(bar(B_EMPTY + s), ((i / kStages) & 1) ^ 1, err)) break;
-        mbar_expect_tx(bar(B_FULL + s), 2 * kTile);
-        const int p0 = (st0 + i) * kPagesPerTile;
+      // ring slot j: K tile j for j < nt, then V tile j - nt
+      for (int j = 0; j < 2 * nt; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(bar(B_EMPTY + s), ((j / kStages) & 1) ^ 1, err)) break;
+        mbar_expect_tx(bar(B_FULL + s), kTile);
+        const bool is_v = j >= nt;
+        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+        const int p0 = (st0 + (is_v ? j - nt : j)) * kPagesPerTile;
 #pragma unroll 1
         for (int p = 0; p < kPagesPerTile; ++p) {
           int id = page_id(pt, p0 + p, max_pages, n_pages);
           if (id < 0) id = 0;   // keys of such a page are masked by the softmax warps
           const int y = (id * n_kv + g) * kPage;
-          const uint32_t dk = sbase + kOffK + s * kTile + p * (kPage * 128);
-          const uint32_t dv = sbase + kOffV + s * kTile + p * (kPage * 128);
-          tma_load_2d(dk, &tm_k, bar(B_FULL + s), 0, y);
-          tma_load_2d(dk + kHalf, &tm_k, bar(B_FULL + s), 64, y);
-          tma_load_2d(dv, &tm_v, bar(B_FULL + s), 0, y);
-          tma_load_2d(dv + kHalf, &tm_v, bar(B_FULL + s), 64, y);
+          const uint32_t dst = sbase + kOffRing + s * kTile + p * (kPage * 128);
+          tma_load_2d(dst, tm, bar(B_FULL + s), 0, y);
+          tma_load_2d(dst + kHalf, tm, bar(B_FULL + s), 64, y);
         }
         ++issued;
       }
@@ -214,154 +200,124 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       bool ok = mbar_wait(bar(B_Q), 0, err);
-      auto issue_s = [&](int i) -> bool {
-        const int s = i % kStages;
-        if (!mbar_wait(bar(B_FULL + s), (i / kStages) & 1, err)) return false;
+      for (int j = 0; j < 2 * nt && ok; ++j) {
+        const int s = j % kStages;
+        if (j == nt) {   // every score tile done: wait for the softmax's P tiles
+          tc_commit(bar(B_SFULL));
+          if (!(ok = mbar_wait(bar(B_PFULL), 0, err))) break;
+        }
+        if (!(ok = mbar_wait(bar(B_FULL + s), (j / kStages) & 1, err))) break;
         tc_fence_after();
-        const uint32_t kb = sbase + kOffK + s * kTile;
+        const uint32_t tb = sbase + kOffRing + s * kTile;
+        if (j < nt) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
-          tc_mma(tmem + 16 * (i & 1), desc_kmajor_sw128(kb + off),
-                 desc_kmajor_sw128(sbase + kOffQ + qoff), kIdescS, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(B_SFULL + (i & 1)));
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      if (ok && n_tiles > 1) ok = issue_s(1);
-      for (int i = 0; i < n_tiles && ok; ++i) {
-        const int h = i & 1;
-        if (i + 2 < n_tiles) {   // score buffer h is free once the softmax has read tile i
-          if (!mbar_wait(bar(B_SFREE + h), (i >> 1) & 1, err)) break;
-          if (!(ok = issue_s(i + 2))) break;
-        }
-        if (!mbar_wait(bar(B_PFULL + h), (i >> 1) & 1, err)) break;
-        tc_fence_after();
-        const uint32_t vb = sbase + kOffV + (i % kStages) * kTile;
-        const uint32_t pb = sbase + kOffP + h * kPBytes;
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
+            tc_mma(tmem + 16 * j, desc_kmajor_sw128(tb + off),
+                   desc_kmajor_sw128(sbase + kOffQ + qoff), kIdescS, kk > 0 ? 1u : 0u);
+          }
+        } else {
+          const int i = j - nt;
+          const uint32_t pb = sbase + kOffP + i * kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {   // 16 keys per MMA
-          tc_mma(tmem + 32, desc_mnmajor_sw128(vb + kk * 2048, kHalf),
-                 desc_kmajor_sw128(pb + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32), kIdescPV,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {   // 16 keys per MMA
+            tc_mma(tmem + kTmemO, desc_mnmajor_sw128(tb + kk * 2048, kHalf),
+                   desc_kmajor_sw128(pb + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32), kIdescPV,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+          }
         }
-        tc_commit(bar(B_EMPTY + (i % kStages)));
-        tc_commit(bar(B_PVDONE + h));
+        tc_commit(bar(B_EMPTY + s));
       }
+      if (ok) tc_commit(bar(B_ODONE));
       tc_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, nullptr);
     }
   } else {
     // ---------------------------------------------------------------- softmax, key per thread
     const int quarter = warp & 3;
-    const int t = quarter * 32 + lane;                  // key of the tile, TMEM lane
+    const int t = quarter * 32 + lane;                  // key of every tile, TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = bar_and(2, 128, mbar_wait(bar(B_SFULL), 0, err));
     float m[G], lsum[G];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      m[hh] = -INFINITY;
-      lsum[hh] = 0.f;
-    }
-    bool ok = true;
-    int last = -1;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int h = i & 1;
-      if (!bar_and(2, 128, mbar_wait(bar(B_SFULL + h), (i >> 1) & 1, err))) {
-        ok = false;
-        break;
-      }
+    float s[kTilesPerSplit][G];
+    if (ok) {
       tc_fence_after();
-      float s[16];
-      tmem_ld16(tmem + 16 * h + lane_off, s);
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE + h));
-      const int kj = (st0 + i) * kTileKeys + t;
-      bool vis = kj >= lo && kj < n;
-      if (vis && page_id(pt, kj / kPage, max_pages, n_pages) < 0) {
-        set_error(err, CC_DEV_CHECK);
-        vis = false;
+      bool bad_page = false;
+#pragma unroll
+      for (int i = 0; i < kTilesPerSplit; ++i) {
+        if (i < nt) {
+          float v[16];
+          tmem_ld16(tmem + 16 * i + lane_off, v);
+          const int kj = (st0 + i) * kTileKeys + t;
+          bool vis = kj >= lo && kj < n;
+          if (vis && page_id(pt, kj / kPage, max_pages, n_pages) < 0) {
+            bad_page = true;
+            vis = false;
+          }
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) s[i][hh] = vis ? v[hh] * scale_log2 : -INFINITY;
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) s[i][hh] = -INFINITY;
+        }
       }
-      // per-head maximum of the tile: warp shuffles, then the four warps via shared memory
-      float* rb = red + h * 64;
+      if (bad_page) set_error(err, CC_DEV_CHECK);
+      // the split's maximum of every head
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        s[hh] = vis ? s[hh] * scale_log2 : -INFINITY;
-        float x = s[hh];
+        float x = s[0][hh];
+#pragma unroll
+        for (int i = 1; i < kTilesPerSplit; ++i) x = fmaxf(x, s[i][hh]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) rb[quarter * 16 + hh] = x;
+        if (lane == 0) red[quarter * 16 + hh] = x;
       }
-      named_barrier_sync(1, 128);
-      bool need_o = false;
-      float f[G];
+    }
+    named_barrier_sync(1, 128);
+    if (ok) {
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        const float mt = fmaxf(fmaxf(rb[hh], rb[16 + hh]), fmaxf(rb[32 + hh], rb[48 + hh]));
-        f[hh] = 1.f;
-        if (mt > m[hh] + kRescaleThreshold) {   // uniform across the CTA
-          if (m[hh] != -INFINITY) {
-            f[hh] = ex2f(m[hh] - mt);
-            need_o = true;
-          }
-          m[hh] = mt;
-        }
+        const float mx = fmaxf(fmaxf(red[hh], red[16 + hh]), fmaxf(red[32 + hh], red[48 + hh]));
+        m[hh] = mx;
+        lsum[hh] = 0.f;
       }
-      if (need_o) {
-        // O^T holds the P V of earlier tiles: wait for the last one, rescale in TMEM
-        if (!bar_and(2, 128, mbar_wait(bar(B_PVDONE + (h ^ 1)), ((i - 1) >> 1) & 1, err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float o[16];
-        tmem_ld16(tmem + 32 + lane_off, o);
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) o[hh] *= f[hh];
-        tmem_st16(tmem + 32 + lane_off, o);
-        tmem_st_wait();
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) lsum[hh] *= f[hh];
-      }
-      // P buffer h was read by PV(i-2)
-      if (i >= 2 && !bar_and(2, 128, mbar_wait(bar(B_PVDONE + h), ((i - 2) >> 1) & 1, err))) {
-        ok = false;
-        break;
-      }
-      // P[hh][t] (row hh, key t) in the 128-byte-swizzled [16 x 128] bf16 buffer
-      const uint32_t pb = sbase + kOffP + h * kPBytes + (t >> 6) * (kPBytes / 2);
+      // P tiles: row hh (head), key t of the 128-byte-swizzled [16 x 128] bf16 buffer
       const int ch = (t & 63) >> 3;
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        const float p = ex2f(s[hh] - (m[hh] == -INFINITY ? 0.f : m[hh]));
-        lsum[hh] += p;
-        const uint32_t addr = pb + hh * 128 + ((ch ^ (hh & 7)) << 4) + ((t & 7) << 1);
-        const __nv_bfloat16 pv = __float2bfloat16_rn(p);
-        asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(*reinterpret_cast<const unsigned short*>(&pv))
-                     : "memory");
+      for (int i = 0; i < kTilesPerSplit; ++i) {
+        if (i >= nt) break;
+        const uint32_t pb = sbase + kOffP + i * kPBytes + (t >> 6) * (kPBytes / 2);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float p = ex2f(s[i][hh] - (m[hh] == -INFINITY ? 0.f : m[hh]));
+          lsum[hh] += p;
+          const uint32_t addr = pb + hh * 128 + ((ch ^ (hh & 7)) << 4) + ((t & 7) << 1);
+          const __nv_bfloat16 pv = __float2bfloat16_rn(p);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
+                       "h"(*reinterpret_cast<const unsigned short*>(&pv))
+                       : "memory");
+        }
       }
       fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL + h));
-      last = i;
     }
-    if (ok && last >= 0)
-      ok = bar_and(2, 128, mbar_wait(bar(B_PVDONE + (last & 1)), (last >> 1) & 1, err));
-    // sum the per-key partial sums over the 128 threads
-    named_barrier_sync(1, 128);
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      float x = lsum[hh];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-      if (lane == 0) red[quarter * 16 + hh] = x;
-    }
-    named_barrier_sync(1, 128);
-    tc_fence_after();
+    mbar_arrive(bar(B_PFULL));
+    named_barrier_sync(1, 128);   // every thread has read the maxima from `red`
     if (ok) {
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        float x = lsum[hh];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        if (lane == 0) red[quarter * 16 + hh] = x;
+      }
+    }
+    named_barrier_sync(1, 128);
+    if (ok) ok = bar_and(2, 128, mbar_wait(bar(B_ODONE), 0, err));
+    if (ok) {
+      tc_fence_after();
       float o[16];
-      tmem_ld16(tmem + 32 + lane_off, o);   // lane t holds dim t of every head
+      tmem_ld16(tmem + kTmemO + lane_off, o);   // lane t holds dim t of every head
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
         const size_t pb2 = part_base + (size_t)hh * splits;
@@ -376,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0 && lane == 0) {
     // a failed launch may leave loads in flight: let them land (bounded)
-    for (int i = max(0, issued - kStages); i < issued; ++i)
-      mbar_wait(bar(B_FULL + (i % kStages)), (i / kStages) & 1, nullptr);
+    for (int j = max(0, issued - kStages); j < issued; ++j)
+      mbar_wait(bar(B_FULL + (j % kStages)), (j / kStages) & 1, nullptr);
   }
   __syncthreads();
   if (warp == 1) {
