@@ -6,6 +6,7 @@
 //              + K/V into the paged cache, + SwiGLU) -> attention -> [o|down] projection
 //              + residual (+ deepstack rows after the first layers)
 //   head       LayerNorm_f on the selected rows -> tied embedding GEMM x logit_scale.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -361,6 +362,13 @@ extern "C" cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_l
 extern "C" void cc_layer_plan_destroy(cc_layer_plan* plan) { delete plan; }
 
 // one GEMM with the plan's tile choice; `b128`/`b256` are the weight maps
+// Rows declared in the tensor map of a workspace activation (a, a2) for an m-row GEMM: at
+// least one 128-row tile of real memory, so a short m (the head's last token, a decode
+// batch) is fetched as plain rows instead of a mostly out-of-bounds box, which the TMA
+// fills far more slowly. Rows past m hold stale data; they only reach accumulator rows the
+// epilogues never store.
+static int act_rows(const cc_layer_plan* p, int m) { return std::max(m, std::min(128, p->T_max)); }
+
 static cc_status plan_gemm(const CUtensorMap& ta, const CUtensorMap& b128, const CUtensorMap& b256,
                            int M, int N, int K, int epi, const EpiParams& ep, int* err,
                            cudaStream_t s) {
@@ -383,8 +391,8 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
   CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, c.sliding_window, p->tiles_s, p->n_tiles, s));
   CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, 0, p->tiles_f, p->n_tiles + 1, s));
   CUtensorMap ta, ta2, tq, tk, tv;
-  if (!make_tmap_bf16_2d(&ta, p->a, T, p->H, p->H, 128, 64) ||
-      !make_tmap_bf16_2d(&ta2, p->a2, T, p->K2, p->K2, 128, 64) ||
+  if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, T), p->H, p->H, 128, 64) ||
+      !make_tmap_bf16_2d(&ta2, p->a2, act_rows(p, T), p->K2, p->K2, 128, 64) ||
       !make_tmap_bf16_2d(&tq, p->q, T, p->q_cols, p->q_cols, 128, 64) ||
       !make_tmap_bf16_2d(&tk, p->k, T, p->kv_cols, p->kv_cols, attn_kv_box_rows(), 64) ||
       !make_tmap_bf16_2d(&tv, p->v, T, p->kv_cols, p->kv_cols, attn_kv_box_rows(), 64))
@@ -523,8 +531,8 @@ extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32
   CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_decode(seq_lens, batch, page_table, max_pages, c.kv_page_size,
                                          kv->n_pages, p->kv_slot, p->n_keys, p->err, s));
   CUtensorMap ta, ta2;
-  if (!make_tmap_bf16_2d(&ta, p->a, batch, p->H, p->H, 128, 64) ||
-      !make_tmap_bf16_2d(&ta2, p->a2, batch, p->K2, p->K2, 128, 64))
+  if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, batch), p->H, p->H, 128, 64) ||
+      !make_tmap_bf16_2d(&ta2, p->a2, act_rows(p, batch), p->K2, p->K2, 128, 64))
     return CC_ERR_CUDA;
   for (int i = 0; i < c.num_layers; ++i) {
     const bool sliding = p->types[i] == CC_SLIDING;
@@ -571,7 +579,7 @@ extern "C" cc_status cc_logits(cc_layer_plan* p, const float* hidden, const int3
     CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(p->final_ln),
                                           p->a, n_rows, p->H, c.layer_norm_eps, rows, s));
     CUtensorMap ta;
-    if (!make_tmap_bf16_2d(&ta, p->a, n_rows, p->H, p->H, 128, 64)) return CC_ERR_CUDA;
+    if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, n_rows), p->H, p->H, 128, 64)) return CC_ERR_CUDA;
     EpiParams e;
     e.c = logits;
     e.ldc = p->V;

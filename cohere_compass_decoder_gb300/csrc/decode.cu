@@ -48,7 +48,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffRing = 4096;                // 1024-aligned
 constexpr uint32_t kOffP = kOffRing + kStages * kTile;
 constexpr uint32_t kOffRed = kOffP + kTilesPerSplit * kPBytes;   // [4 warps][16] floats
-constexpr uint32_t kOffBar = kOffRed + 4 * 16 * 4;
+constexpr uint32_t kOffPid = kOffRed + 4 * 16 * 4;              // the split's page ids
+constexpr uint32_t kOffBar = kOffPid + kPagesPerSplit * 4;
 constexpr size_t kSmem = 1024 + kOffBar + 256;
 constexpr uint32_t kTmemCols = 256;                // S^T of 8 tiles (16 columns each) | O^T
 constexpr uint32_t kTmemO = 16 * kTilesPerSplit;
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
   float* red = reinterpret_cast<float*>(smem + kOffRed);
+  int* pid = reinterpret_cast<int*>(smem + kOffPid);
   const int32_t* pt = page_table + (size_t)b * max_pages;
 
   const int warp = warp_id(), lane = lane_id();
@@ -157,6 +159,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // the split's page ids, read once: the producer's gathers and the masks use this copy
+  if (threadIdx.x < kPagesPerSplit)
+    pid[threadIdx.x] = page_id(pt, st0 * kPagesPerTile + threadIdx.x, max_pages, n_pages);
   // P rows G..15 are padding: zero them in every tile buffer
   if (G < kQRows) {
     for (int i = threadIdx.x; i < kTilesPerSplit * kPBytes / 16; i += kThreads) {
@@ -184,11 +189,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_expect_tx(bar(B_FULL + s), kTile);
         const bool is_v = j >= nt;
         const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-        const int p0 = (st0 + (is_v ? j - nt : j)) * kPagesPerTile;
-#pragma unroll 1
+        const int p0 = (is_v ? j - nt : j) * kPagesPerTile;
+#pragma unroll
         for (int p = 0; p < kPagesPerTile; ++p) {
-          int id = page_id(pt, p0 + p, max_pages, n_pages);
-          if (id < 0) id = 0;   // keys of such a page are masked by the softmax warps
+          const int id = max(pid[p0 + p], 0);   // keys of an invalid page are masked below
           const int y = (id * n_kv + g) * kPage;
           const uint32_t dst = sbase + kOffRing + s * kTile + p * (kPage * 128);
           tma_load_2d(dst, tm, bar(B_FULL + s), 0, y);
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_ld16(tmem + 16 * i + lane_off, v);
           const int kj = (st0 + i) * kTileKeys + t;
           bool vis = kj >= lo && kj < n;
-          if (vis && page_id(pt, kj / kPage, max_pages, n_pages) < 0) {
+          if (vis && pid[i * kPagesPerTile + t / kPage] < 0) {
             bad_page = true;
             vis = false;
           }
