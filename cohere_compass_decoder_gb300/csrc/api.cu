@@ -176,6 +176,13 @@ struct cc_layer_plan {
   int32_t *ds_map = nullptr, *kv_slot = nullptr, *n_keys = nullptr, *n_tiles = nullptr;
   AttnTile *tiles_s = nullptr, *tiles_f = nullptr;
   int max_tiles = 0;
+  // prefill attention: partials of split query tiles, then [arrival counters | one item
+  // counter per layer], zeroed before each forward
+  float* attn_part_o = nullptr;
+  float2* attn_part_ml = nullptr;
+  int32_t* attn_cnt = nullptr;
+  size_t attn_cnt_ints = 0;
+  int attn_groups_n = 1;
   // decode split-KV scratch, grown on demand
   float* dec_scratch = nullptr;
   size_t dec_scratch_floats = 0;
@@ -306,6 +313,13 @@ extern "C" cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_l
   parts.push_back({reinterpret_cast<void**>(&p->tiles_s), p->max_tiles * sizeof(AttnTile)});
   parts.push_back({reinterpret_cast<void**>(&p->tiles_f), p->max_tiles * sizeof(AttnTile)});
   if (p->bf16) {
+    p->attn_groups_n = attn_groups(p->nq, p->nkv);
+    p->attn_cnt_ints = (size_t)attn_counter_ints(p->attn_groups_n) + cfg->num_layers;
+    parts.push_back({reinterpret_cast<void**>(&p->attn_part_o),
+                     attn_part_o_floats(p->nq, p->nkv) * sizeof(float)});
+    parts.push_back({reinterpret_cast<void**>(&p->attn_part_ml),
+                     attn_part_ml_pairs(p->nq, p->nkv) * sizeof(float2)});
+    parts.push_back({reinterpret_cast<void**>(&p->attn_cnt), p->attn_cnt_ints * 4});
     parts.push_back({reinterpret_cast<void**>(&p->a), T * p->H * 2});
     parts.push_back({reinterpret_cast<void**>(&p->q), T * p->q_cols * 2});
     parts.push_back({reinterpret_cast<void**>(&p->k), T * p->kv_cols * 2});
@@ -388,8 +402,12 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
   if (kv)
     CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_prefill(cu, n_seqs, T, page_table, max_pages, c.kv_page_size,
                                             kv->n_pages, p->kv_slot, p->err, s));
-  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, c.sliding_window, p->tiles_s, p->n_tiles, s));
-  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, 0, p->tiles_f, p->n_tiles + 1, s));
+  // both work lists (sliding, full) in one launch, which also clears the attention counters
+  CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, p->attn_groups_n, c.sliding_window,
+                                                 p->tiles_s, p->n_tiles, 0, p->tiles_f,
+                                                 p->n_tiles + 1, p->attn_cnt,
+                                                 static_cast<int>(p->attn_cnt_ints), s));
+  const int32_t* layer_sched0 = p->attn_cnt + (p->attn_cnt_ints - c.num_layers);
   CUtensorMap ta, ta2, tq, tk, tv;
   if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, T), p->H, p->H, 128, 64) ||
       !make_tmap_bf16_2d(&ta2, p->a2, act_rows(p, T), p->K2, p->K2, 128, 64) ||
@@ -422,9 +440,14 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
     e1.ld_act = p->K2;
     CC_TIMED(p, CC_K_GEMM_QKV_MLP, s, plan_gemm(ta, p->w1_128[i], p->w1_256[i], T, p->N1, p->H, EPI_QKV_MLP, e1,
                               p->err, s));
+    AttnScratch sc;
+    sc.part_o = p->attn_part_o;
+    sc.part_ml = p->attn_part_ml;
+    sc.counters = p->attn_cnt;
+    sc.sched = const_cast<int32_t*>(layer_sched0) + i;
     CC_TIMED(p, CC_K_ATTN_PREFILL, s, launch_attn_prefill(tq, tk, tv, p->a2, p->K2, sliding ? p->tiles_s : p->tiles_f,
                                         p->n_tiles + (sliding ? 0 : 1), tiles, p->nq, p->nkv,
-                                        sliding ? c.sliding_window : 0, p->err, s));
+                                        sliding ? c.sliding_window : 0, sc, p->err, s));
     EpiParams e2;
     e2.c = hidden;
     e2.ldc = p->H;
@@ -665,15 +688,29 @@ extern "C" cc_status cc_op_attention_prefill(const void* q, const void* k, const
       !make_tmap_bf16_2d(&tv, v, tokens, n_kv * 128, n_kv * 128, attn_kv_box_rows(), 64))
     return CC_ERR_INVALID_ARG;
   const int max_tiles = attn_max_tiles(tokens, n_seqs);
+  const int groups = attn_groups(n_q, n_kv);
+  // one stream-ordered allocation: [n_tiles | split counters, item counter | tiles |
+  // partial (max, sum) | partial O]
+  const size_t cnt_ints = (size_t)attn_counter_ints(groups) + 1;
+  const size_t off_tiles = align256(256 + cnt_ints * 4);
+  const size_t off_ml = align256(off_tiles + (size_t)max_tiles * sizeof(AttnTile));
+  const size_t off_o = align256(off_ml + attn_part_ml_pairs(n_q, n_kv) * sizeof(float2));
+  const size_t bytes = off_o + attn_part_o_floats(n_q, n_kv) * sizeof(float);
   void* scratch = nullptr;
-  const size_t bytes = 256 + (size_t)max_tiles * sizeof(AttnTile);
   CC_CHECK_CUDA(cudaMallocAsync(&scratch, bytes, s));
-  int32_t* n_tiles = static_cast<int32_t*>(scratch);
-  AttnTile* tiles = reinterpret_cast<AttnTile*>(static_cast<uint8_t*>(scratch) + 256);
-  cc_status st = launch_attn_tiles(cu_seqlens, n_seqs, tokens, window, tiles, n_tiles, s);
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  int32_t* n_tiles = reinterpret_cast<int32_t*>(base);
+  AttnScratch sc;
+  sc.counters = reinterpret_cast<int32_t*>(base + 256);
+  sc.sched = sc.counters + (cnt_ints - 1);
+  sc.part_ml = reinterpret_cast<float2*>(base + off_ml);
+  sc.part_o = reinterpret_cast<float*>(base + off_o);
+  AttnTile* tiles = reinterpret_cast<AttnTile*>(base + off_tiles);
+  cc_status st = launch_attn_tiles(cu_seqlens, n_seqs, tokens, groups, window, tiles, n_tiles, 0,
+                                   nullptr, nullptr, sc.counters, static_cast<int>(cnt_ints), s);
   if (st == CC_OK)
     st = launch_attn_prefill(tq, tk, tv, static_cast<__nv_bfloat16*>(out), ld_out, tiles, n_tiles,
-                             max_tiles, n_q, n_kv, window, op_error_flag(), s);
+                             max_tiles, n_q, n_kv, window, sc, op_error_flag(), s);
   CC_CHECK_CUDA(cudaFreeAsync(scratch, s));
   return st;
 }

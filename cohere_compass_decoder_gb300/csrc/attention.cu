@@ -7,11 +7,16 @@
 // (sliding layers: "causal restricted to the last 4096 keys"). Query head h reads KV head
 // h / (n_q / n_kv).
 //
-// One CTA per (128-query tile, pair of query heads that read the same KV head; one head
-// when n_q / n_kv is odd), 10 warps:
-//   warp 0      TMA: the Q tiles once, then K and V tiles of 128 keys x 128 dims (two
-//               64-column boxes, 128-byte swizzle) into 3-stage (K) and 2-stage (V) rings;
-//               each K/V tile feeds both heads
+// Work items: (128-query tile or a chunk of its key tiles, head group), where a head group is
+// the pair of query heads that read the same KV head (a single head when n_q / n_kv is odd).
+// A tile builder lists them heaviest first and cuts a query tile whose key range is long
+// next to the launch's average work per SM into chunks, so that the longest item of a short
+// causal sequence no longer sets the kernel's duration. One persistent CTA per SM takes
+// items in that order from a global counter; 10 warps:
+//   warp 0      scheduler and TMA: takes the next item, hands it to the other warps through
+//               a 2-entry shared-memory queue, loads its Q tiles, then its K and V tiles of
+//               128 keys x 128 dims (two 64-column boxes, 128-byte swizzle) into 3-stage (K)
+//               and 2-stage (V) rings; each K/V tile feeds both heads
 //   warp 1      MMA: S_h = Q_h K^T (M=128, N=128) into the head's TMEM score region, and
 //               O_h += P_h V with P_h read from tensor memory (M=128, N=128, V MN-major)
 //   warps 2..5  softmax of head 0, warps 6..9 softmax of head 1: one query row per thread,
@@ -26,6 +31,11 @@
 // bf16 first and the result is the bf16 P the P V MMA consumes anyway; the row sums add
 // exactly those bf16 values. Key tiles wholly outside the causal/window band are never
 // loaded.
+// A chunk of a split tile stores (max, sum, O) of each of its rows in fp32 and counts itself
+// in the tile's arrival counter; the chunk that arrives last merges all partials in chunk
+// order (the same arithmetic whichever chunk is last) and writes the bf16 rows.
+#include <algorithm>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -36,36 +46,47 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kKeys = 128;                             // keys per tile
 constexpr int kKStages = 3, kVStages = 2;
+constexpr int kMinChunk = 6;                           // key tiles: never split below this
+constexpr int kMergeTiles = 6;                         // a merge costs about this many tiles
+constexpr int kMaxChunks = 8;                          // chunks of one split query tile
+constexpr int kCounterInts = 1 + kMaxChunks;           // arrival count, ready flags
 constexpr uint32_t kTile = 128 * 128 * 2;              // 32 KB: 128 rows x 128 dims
 constexpr uint32_t kHalf = 128 * 64 * 2;               // one 64-dim box column: 16 KB
 constexpr uint32_t kOffQ = 0;                          // 2 heads
 constexpr uint32_t kOffK = kOffQ + 2 * kTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
-constexpr size_t kSmem = 1024 + kOffBar + 256;
+constexpr uint32_t kBarBytes = 256;                    // barriers, TMEM slot, item queue
+constexpr uint32_t kOffRed = kOffBar + kBarBytes;      // [2][2 halves][128 rows] fp32 maxima
+constexpr size_t kSmem = kOffRed + 2 * 2 * 128 * 4;   // the dynamic base is 1024-aligned
 constexpr uint32_t kTmemCols = 512;  // head h: scores / P at 256 h, output at 256 h + 128
 constexpr uint32_t kIdescS = idesc_bf16(128, kKeys, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
+constexpr int kSoftmaxWarps = 8;
 
 enum {
-  B_Q = 0,
-  B_KFULL = 1, B_KEMPTY = B_KFULL + kKStages, B_VFULL = B_KEMPTY + kKStages,
+  B_Q = 0,        // Q tiles of the current item loaded
+  B_QEMPTY,       // the current item's last scores are done with Q
+  B_KFULL, B_KEMPTY = B_KFULL + kKStages, B_VFULL = B_KEMPTY + kKStages,
   B_VEMPTY = B_VFULL + kVStages,
   B_SFULL = B_VEMPTY + kVStages,  // [head]: scores of the head's current tile ready
-  B_PFULL = B_SFULL + 2,          // [head], 128 arrivals: P of the head's current tile in TMEM
+  B_PFULL = B_SFULL + 2,          // [head], 256 arrivals: P of the head's current tile in TMEM
   B_ODONE = B_PFULL + 2,          // [head]: P V of the head's tiles
-  B_DRAIN = B_ODONE + 2,
+  B_IFULL = B_ODONE + 2,          // [2]: item queue entry written
+  B_IEMPTY = B_IFULL + 2,         // [2], 1 + 8 arrivals: entry read by the MMA and softmax warps
+  B_DRAIN = B_IEMPTY + 2,
   B_COUNT = B_DRAIN + 1
 };
+// after the barriers: TMEM base (4 B), item queue (2 x 4 B), merge flag (4 B)
+static_assert(8 * B_COUNT + 16 <= kBarBytes, "barrier area");
 
 __device__ __forceinline__ float ex2_mufu(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
 
 // 2^x of two bf16 values packed in one register (low half first), bf16 results.
 __device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
@@ -80,34 +101,104 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier over `threads` threads that also ANDs a predicate across them.
+__device__ __forceinline__ bool bar_and(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// Loads that bypass L1: the partials of other CTAs are read once, after their arrival count.
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float2 ld_cg_f2(const float2* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CC_R8(0), CC_R8(8)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits (bounded, like the barrier waits) until another CTA has set *flag; that CTA has
+// already counted its arrival, so it is running and only stores before setting it.
+__device__ __forceinline__ bool wait_flag(const int* flag, int* err) {
+  const long long t0 = clock64();
+  for (uint32_t n = 0;; ++n) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0) return true;
+    if ((n & 63u) == 63u) {
+      if (*reinterpret_cast<volatile int*>(err) != 0) return false;
+      if (clock64() - t0 > kWaitTimeoutCycles) {
+        set_error(err, CC_DEV_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_prefill(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                    int ld_out, const AttnTile* __restrict__ tiles, const int32_t* n_tiles_p,
-                   int n_q, int n_kv, int window, float scale_log2, int* err) {
-  if (static_cast<int>(blockIdx.x) >= *n_tiles_p) return;
-  const AttnTile tile = tiles[blockIdx.x];
+                   int n_q, int n_kv, int window, float scale_log2, AttnScratch sc, int* err) {
   const int G = n_q / n_kv;
   const bool paired = (G & 1) == 0;                    // two heads share this KV head
   const int nh = paired ? 2 : 1;
-  const int head0 = paired ? 2 * blockIdx.y : blockIdx.y;
-  const int kvh = head0 / G;
-  const int q0 = tile.q0;
-  const int q_last = min(q0 + 127, tile.seq_len - 1);
-  const int kt_hi = q_last / kKeys;
-  const int kt_lo = window > 0 ? max(0, q0 - window + 1) / kKeys : 0;
-  const int n = kt_hi - kt_lo + 1;                     // key tiles
+  const int groups = paired ? n_q / 2 : n_q;
+  const int n_items = *n_tiles_p * groups;
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
+  // the 128-byte-swizzled tiles need a 1024-byte aligned base; the kernel keeps no slack for
+  // realigning, so a misplaced base is reported instead of used
+  if ((sbase & 1023u) != 0) {
+    if (threadIdx.x == 0) set_error(err, CC_DEV_CHECK);
+    return;
+  }
   auto bar = [&](int i) { return sbase + kOffBar + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
+  volatile int* queue = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT + 4);
+  volatile int* merge_flag = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * B_COUNT + 12);
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q), 1);
+    mbar_init(bar(B_QEMPTY), 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
@@ -118,8 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(B_SFULL + h), 1);
-      mbar_init(bar(B_PFULL + h), 128);
+      mbar_init(bar(B_PFULL + h), 32 * kSoftmaxWarps);
       mbar_init(bar(B_ODONE + h), 1);
+      mbar_init(bar(B_IFULL + h), 1);
+      mbar_init(bar(B_IEMPTY + h), 1 + kSoftmaxWarps);
     }
     mbar_init(bar(B_DRAIN), 1);
     fence_mbar_init();
@@ -136,43 +229,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   int issued_k = 0, issued_v = 0;
   if (warp == 0) {
     if (lane == 0) {
-      const int kx = kvh * 128;
-      mbar_expect_tx(bar(B_Q), nh * kTile);
-      for (int h = 0; h < nh; ++h) {
-        const int qx = (head0 + h) * 128;
-        tma_load_2d(sbase + kOffQ + h * kTile, &tm_q, bar(B_Q), qx, tile.seq_start + q0);
-        tma_load_2d(sbase + kOffQ + h * kTile + kHalf, &tm_q, bar(B_Q), qx + 64,
-                    tile.seq_start + q0);
-      }
-      // K runs up to three tiles ahead, V up to two
-      int tk = 0, tv = 0;
-      while ((tk < n || tv < n)) {
-        if (tk < n && tk <= tv + 1) {
-          const int st = tk % kKStages;
-          if (!mbar_wait(bar(B_KEMPTY + st), ((tk / kKStages) & 1) ^ 1, err)) break;
-          const int y = tile.seq_start + (kt_lo + tk) * kKeys;
-          mbar_expect_tx(bar(B_KFULL + st), kTile);
-          tma_load_2d(sbase + kOffK + st * kTile, &tm_k, bar(B_KFULL + st), kx, y);
-          tma_load_2d(sbase + kOffK + st * kTile + kHalf, &tm_k, bar(B_KFULL + st), kx + 64, y);
-          ++tk;
-          ++issued_k;
-        } else {
-          const int st = tv % kVStages;
-          if (!mbar_wait(bar(B_VEMPTY + st), ((tv / kVStages) & 1) ^ 1, err)) break;
-          const int y = tile.seq_start + (kt_lo + tv) * kKeys;
-          mbar_expect_tx(bar(B_VFULL + st), kTile);
-          tma_load_2d(sbase + kOffV + st * kTile, &tm_v, bar(B_VFULL + st), kx, y);
-          tma_load_2d(sbase + kOffV + st * kTile + kHalf, &tm_v, bar(B_VFULL + st), kx + 64, y);
-          ++tv;
-          ++issued_v;
+      // ------------------------------------------------------------ scheduler + TMA
+      for (int j = 0;; ++j) {
+        const int e = j & 1;
+        if (!mbar_wait(bar(B_IEMPTY + e), ((j >> 1) & 1) ^ 1, err)) break;
+        // the first item of every CTA is its index, later ones come from the counter
+        int u = j == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(sc.sched, 1);
+        if (u >= n_items) u = -1;
+        queue[e] = u;
+        mbar_arrive(bar(B_IFULL + e));
+        if (u < 0) break;
+        const AttnTile tile = tiles[u / groups];
+        const int head0 = (u % groups) * nh;
+        const int kx = (head0 / G) * 128;
+        const int n = tile.kt1 - tile.kt0;
+        // Q of this item once the previous item's last scores no longer read it
+        if (!mbar_wait(bar(B_QEMPTY), (j & 1) ^ 1, err)) break;
+        mbar_expect_tx(bar(B_Q), nh * kTile);
+        for (int h = 0; h < nh; ++h) {
+          const int qx = (head0 + h) * 128;
+          tma_load_2d(sbase + kOffQ + h * kTile, &tm_q, bar(B_Q), qx, tile.seq_start + tile.q0);
+          tma_load_2d(sbase + kOffQ + h * kTile + kHalf, &tm_q, bar(B_Q), qx + 64,
+                      tile.seq_start + tile.q0);
         }
+        // K runs up to one tile ahead of V within the item
+        bool ok = true;
+        for (int a = 0, b = 0; a < n || b < n;) {
+          if (a < n && a <= b + 1) {
+            const int st = issued_k % kKStages;
+            if (!(ok = mbar_wait(bar(B_KEMPTY + st), ((issued_k / kKStages) & 1) ^ 1, err))) break;
+            const int y = tile.seq_start + (tile.kt0 + a) * kKeys;
+            mbar_expect_tx(bar(B_KFULL + st), kTile);
+            tma_load_2d(sbase + kOffK + st * kTile, &tm_k, bar(B_KFULL + st), kx, y);
+            tma_load_2d(sbase + kOffK + st * kTile + kHalf, &tm_k, bar(B_KFULL + st), kx + 64, y);
+            ++a;
+            ++issued_k;
+          } else {
+            const int st = issued_v % kVStages;
+            if (!(ok = mbar_wait(bar(B_VEMPTY + st), ((issued_v / kVStages) & 1) ^ 1, err))) break;
+            const int y = tile.seq_start + (tile.kt0 + b) * kKeys;
+            mbar_expect_tx(bar(B_VFULL + st), kTile);
+            tma_load_2d(sbase + kOffV + st * kTile, &tm_v, bar(B_VFULL + st), kx, y);
+            tma_load_2d(sbase + kOffV + st * kTile + kHalf, &tm_v, bar(B_VFULL + st), kx + 64, y);
+            ++b;
+            ++issued_v;
+          }
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait(bar(B_Q), 0, err);
-      auto issue_s = [&](int h, int t) {
-        const uint32_t kb = sbase + kOffK + (t % kKStages) * kTile;
+      // ------------------------------------------------------------ MMA
+      auto issue_s = [&](int h, int g) {   // scores of head h against K tile g (CTA count)
+        const uint32_t kb = sbase + kOffK + (g % kKStages) * kTile;
         const uint32_t qb = sbase + kOffQ + h * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -182,146 +292,345 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(bar(B_SFULL + h));
       };
-      if (ok) ok = mbar_wait(bar(B_KFULL + 0), 0, err);
-      if (ok) {
+      bool ok = true;
+      int gt = 0;   // key tiles of this CTA's earlier items
+      for (int j = 0; ok; ++j) {
+        const int e = j & 1;
+        if (!(ok = mbar_wait(bar(B_IFULL + e), (j >> 1) & 1, err))) break;
+        const int u = queue[e];
+        mbar_arrive(bar(B_IEMPTY + e));
+        if (u < 0) break;
+        const AttnTile tile = tiles[u / groups];
+        const int n = tile.kt1 - tile.kt0;
+        if (!(ok = mbar_wait(bar(B_Q), j & 1, err))) break;
+        if (!(ok = mbar_wait(bar(B_KFULL + gt % kKStages), (gt / kKStages) & 1, err))) break;
         tc_fence_after();
-        for (int h = 0; h < nh; ++h) issue_s(h, 0);
-        tc_commit(bar(B_KEMPTY + 0));
-      }
-      for (int t = 0; t < n && ok; ++t) {
-        const bool next = t + 1 < n;
-        for (int h = 0; h < nh && ok; ++h) {
-          // P_h(t) is in TMEM: O_h += P_h V(t), then the head's next scores (same columns)
-          if (!(ok = mbar_wait(bar(B_PFULL + h), t & 1, err))) break;
-          if (h == 0 && !(ok = mbar_wait(bar(B_VFULL + t % kVStages), (t / kVStages) & 1, err)))
-            break;
-          if (h == 0 && next &&
-              !(ok = mbar_wait(bar(B_KFULL + (t + 1) % kKStages), ((t + 1) / kKStages) & 1, err)))
-            break;
-          tc_fence_after();
-          const uint32_t vb = sbase + kOffV + (t % kVStages) * kTile;
+        for (int h = 0; h < nh; ++h) issue_s(h, gt);
+        tc_commit(bar(B_KEMPTY + gt % kKStages));
+        if (n == 1) tc_commit(bar(B_QEMPTY));
+        for (int t = 0; t < n && ok; ++t) {
+          const int g = gt + t;
+          const bool next = t + 1 < n;
+          for (int h = 0; h < nh && ok; ++h) {
+            // P_h(t) is in TMEM: O_h += P_h V(t), then the head's next scores (same columns)
+            if (!(ok = mbar_wait(bar(B_PFULL + h), g & 1, err))) break;
+            if (h == 0 && !(ok = mbar_wait(bar(B_VFULL + g % kVStages), (g / kVStages) & 1, err)))
+              break;
+            if (h == 0 && next &&
+                !(ok = mbar_wait(bar(B_KFULL + (g + 1) % kKStages), ((g + 1) / kKStages) & 1, err)))
+              break;
+            tc_fence_after();
+            const uint32_t vb = sbase + kOffV + (g % kVStages) * kTile;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {   // 16 keys per MMA: 8 packed P columns
-            tc_mma_ts(tmem + 256 * h + 128, tmem + 256 * h + 8 * kk,
-                      desc_mnmajor_sw128(vb + kk * 2048, kHalf), kIdescPV,
-                      (t > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {   // 16 keys per MMA: 8 packed P columns
+              tc_mma_ts(tmem + 256 * h + 128, tmem + 256 * h + 8 * kk,
+                        desc_mnmajor_sw128(vb + kk * 2048, kHalf), kIdescPV,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(bar(B_ODONE + h));
+            if (next) issue_s(h, g + 1);
           }
-          tc_commit(bar(B_ODONE + h));
-          if (next) issue_s(h, t + 1);
+          if (!ok) break;
+          tc_commit(bar(B_VEMPTY + g % kVStages));
+          if (next) tc_commit(bar(B_KEMPTY + (g + 1) % kKStages));
+          if (t == n - 2) tc_commit(bar(B_QEMPTY));   // the item's last scores are issued
         }
-        if (!ok) break;
-        tc_commit(bar(B_VEMPTY + t % kVStages));
-        if (next) tc_commit(bar(B_KEMPTY + (t + 1) % kKStages));
+        gt += n;
       }
       tc_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, nullptr);
     }
   } else {
-    // ---------------------------------------------------------------- softmax groups
-    const int grp = (warp - 2) >> 2;                 // head slot of this group
+    // ------------------------------------------------------------ softmax, all 8 warps
+    // Warp w takes keys 64*half .. 64*half+63 of every score tile (half = 0 for warps 2..5,
+    // 1 for warps 6..9) for the 32 query rows of its TMEM lane quarter; warps w and w+4 share
+    // those rows and combine their partial maxima through shared memory at a pair barrier.
+    // The heads of the item are processed one after the other, so each head's P is ready
+    // after half a tile's work while the tensor cores run the other head's products.
+    const int half = (warp - 2) >> 2;
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;               // query row in the tile
-    const int qi = q0 + r;                           // query index in its sequence
-    // this warp's rows that lie inside the sequence (rows past its end are never stored)
-    const int qw_lo = q0 + quarter * 32, qw_hi = min(qw_lo + 31, tile.seq_len - 1);
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t s_tmem = tmem + 256 * grp + lane_off;
-    const uint32_t o_tmem = s_tmem + 128;
-    float m = -INFINITY, l = 0.f;
-    bool ok = grp < nh;
-    for (int t = 0; t < n && ok; ++t) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + grp), t & 1, err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int kbase = (kt_lo + t) * kKeys;
-      // warp-uniform: every key of the tile visible to every row of this warp
-      const bool full = (kbase + kKeys - 1 <= qw_lo) && (window <= 0 || qw_hi - kbase < window);
-      float s[kKeys];
-      tmem_ld128(s_tmem, s);
-      if (!full) {
-        const int hi_c = qi - kbase;                             // causal: c <= hi_c
-        const int lo_c = window > 0 ? qi - window + 1 - kbase : -1;
+    const int pair_bar = 3 + quarter;                // named barrier of warps (w, w+4)
+    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2 buffers][2 halves][128 rows]
+    // All eight softmax warps take every decision to stop together, at a barrier that ANDs
+    // their status, so none waits at a barrier another left.
+    constexpr int kSmThreads = 32 * kSoftmaxWarps;
+    bool ok = true;
+    int gt = 0;
+    for (int j = 0; ok; ++j) {
+      const int e = j & 1;
+      if (!bar_and(2, kSmThreads, mbar_wait(bar(B_IFULL + e), (j >> 1) & 1, err))) break;
+      const int u = queue[e];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_IEMPTY + e));
+      if (u < 0) break;
+      const AttnTile tile = tiles[u / groups];
+      const int n = tile.kt1 - tile.kt0;
+      const int head0 = (u % groups) * nh;
+      const int q0 = tile.q0;
+      const int qi = q0 + r;                         // query index in its sequence
+      // this warp's rows that lie inside the sequence (rows past its end are never stored)
+      const int qw_lo = q0 + quarter * 32, qw_hi = min(qw_lo + 31, tile.seq_len - 1);
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // l: this half's keys
+      for (int t = 0; t < n && ok; ++t) {
+        const int g = gt + t;
+        const int kbase = (tile.kt0 + t) * kKeys + 64 * half;     // first key of this half
+        // warp-uniform: every key of this half visible to every row of this warp
+        const bool full = (kbase + 63 <= qw_lo) && (window <= 0 || qw_hi - kbase < window);
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) s[c] = (c <= hi_c && c >= lo_c) ? s[c] : -INFINITY;
-      }
-      float a0 = max3(s[0], s[1], s[2]), a1 = max3(s[3], s[4], s[5]);
-      float a2 = max3(s[6], s[7], s[8]), a3 = max3(s[9], s[10], s[11]);
+        for (int h = 0; h < 2; ++h) {
+          if (h >= nh) break;
+          const uint32_t s_tmem = tmem + 256 * h + lane_off;
+          const uint32_t o_tmem = s_tmem + 128 + 64 * half;
+          const bool w_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + h), g & 1, err));
+          float* rb = red + (nh == 2 ? h : (g & 1)) * 256;
+          float s[64];
+          float mp = -INFINITY;
+          if (w_ok) {
+            tc_fence_after();
+            tmem_ld64(s_tmem + 64 * half, s);
+            if (!full) {
+              const int hi_c = qi - kbase;                           // causal: c <= hi_c
+              const int lo_c = window > 0 ? qi - window + 1 - kbase : -1;
 #pragma unroll
-      for (int c = 12; c < 124; c += 8) {
-        a0 = max3(a0, s[c], s[c + 1]);
-        a1 = max3(a1, s[c + 2], s[c + 3]);
-        a2 = max3(a2, s[c + 4], s[c + 5]);
-        a3 = max3(a3, s[c + 6], s[c + 7]);
-      }
-      a0 = max3(a0, s[124], s[125]);
-      a1 = max3(a1, s[126], s[127]);
-      const float mt = fmaxf(max3(a0, a1, a2), a3) * scale_log2;
-      const bool need = mt > m + kRescaleThreshold;  // also true when m == -inf < mt
-      const bool need_o = need && (m != -INFINITY);
-      if (__any_sync(0xffffffffu, need_o)) {
-        // O holds P V of tiles < t, all complete: the scores of tile t were issued after them
-        const float f = need_o ? ex2_mufu(m - mt) : 1.f;
+              for (int c = 0; c < 64; ++c) s[c] = (c <= hi_c && c >= lo_c) ? s[c] : -INFINITY;
+            }
+            float a0 = max3(s[0], s[1], s[2]), a1 = max3(s[3], s[4], s[5]);
+            float a2 = max3(s[6], s[7], s[8]), a3 = max3(s[9], s[10], s[11]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float o[32];
-          tmem_ld32(o_tmem + 32 * c, o);
+            for (int c = 12; c < 60; c += 8) {
+              a0 = max3(a0, s[c], s[c + 1]);
+              a1 = max3(a1, s[c + 2], s[c + 3]);
+              a2 = max3(a2, s[c + 4], s[c + 5]);
+              a3 = max3(a3, s[c + 6], s[c + 7]);
+            }
+            a0 = max3(a0, s[60], s[61]);
+            a1 = max3(a1, s[62], s[63]);
+            mp = fmaxf(max3(a0, a1, a2), a3) * scale_log2;
+            rb[half * 128 + r] = mp;
+          }
+          // both halves have read their scores (P may now overwrite them) and posted maxima
+          if (!bar_and(pair_bar, 64, w_ok)) {
+            ok = false;
+            break;
+          }
+          const float mt = fmaxf(rb[0 * 128 + r], rb[1 * 128 + r]);   // same in both halves
+          const bool need = mt > m[h] + kRescaleThreshold;  // also true when m == -inf < mt
+          const bool need_o = need && (m[h] != -INFINITY);
+          if (__any_sync(0xffffffffu, need_o)) {
+            // O holds P V of tiles < t, all complete: the scores of tile t were issued after
+            const float f = need_o ? ex2_mufu(m[h] - mt) : 1.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
-          tmem_st32(o_tmem + 32 * c, o);
+            for (int c = 0; c < 2; ++c) {
+              float o[32];
+              tmem_ld32(o_tmem + 32 * c, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] *= f;
+              tmem_st32(o_tmem + 32 * c, o);
+            }
+            if (need_o) l[h] *= f;
+          }
+          if (need) m[h] = mt;
+          const float mu = (m[h] == -INFINITY) ? 0.f : m[h];
+          // P = 2^(s * scale_log2 - m) (masked scores are -inf and give 0), its row sum, bf16
+          // P packed two keys per column: this half's keys go to columns 32*half .. +31
+          const float2 sc2 = make_float2(scale_log2, scale_log2);
+          const float2 nm2 = make_float2(-mu, -mu);
+          float2 sum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
+          uint32_t pk[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const float2 x = __ffma2_rn(make_float2(s[2 * jj], s[2 * jj + 1]), sc2, nm2);
+            // two probabilities per MUFU operation, already the bf16 P the P V MMA reads
+            const uint32_t p2 = ex2_bf16x2(pack_bf16x2(x.x, x.y));
+            pk[jj] = p2;
+            sum[jj & 3] = __fadd2_rn(sum[jj & 3], make_float2(__uint_as_float(p2 << 16),
+                                                              __uint_as_float(p2 & 0xFFFF0000u)));
+          }
+          tmem_st32u(s_tmem + 32 * half, pk);
+          l[h] += ((sum[0].x + sum[0].y) + (sum[1].x + sum[1].y)) +
+                  ((sum[2].x + sum[2].y) + (sum[3].x + sum[3].y));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(B_PFULL + h));
         }
-        if (need_o) l *= f;
       }
-      if (need) m = mt;
-      const float mu = (m == -INFINITY) ? 0.f : m;
-      // P = 2^(s * scale_log2 - m) (masked scores are -inf and give 0), its row sum, bf16 P
-      // packed two keys per column over the first 64 score columns
-      const float2 sc2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(-mu, -mu);
-      float2 sum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int h = 0; h < 2; ++h)
+        if (h < nh && ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + h), (gt + n - 1) & 1, err));
+      gt += n;
+      // row sums: both halves add the two partial sums in the same order
+      ok = bar_and(pair_bar, 64, ok);    // the partner has read the last maxima
+      if (ok) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int c = 64 * half + 2 * j;
-          const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
-          // two probabilities per MUFU operation, already the bf16 P the P V MMA reads
-          const uint32_t p2 = ex2_bf16x2(pack_bf16x2(x.x, x.y));
-          pk[j] = p2;
-          sum[j & 3] = __fadd2_rn(sum[j & 3], make_float2(__uint_as_float(p2 << 16),
-                                                          __uint_as_float(p2 & 0xFFFF0000u)));
-        }
-        tmem_st32u(s_tmem + 32 * half, pk);
+        for (int h = 0; h < 2; ++h)
+          if (h < nh) red[h * 256 + half * 128 + r] = l[h];
       }
-      l += ((sum[0].x + sum[0].y) + (sum[1].x + sum[1].y)) +
-           ((sum[2].x + sum[2].y) + (sum[3].x + sum[3].y));
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL + grp));
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + grp), (n - 1) & 1, err));
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      named_barrier_sync(pair_bar, 64);
+      float L[2] = {0.f, 0.f};
+      if (ok) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (h < nh) L[h] = red[h * 256 + r] + red[h * 256 + 128 + r];
+      }
       const bool row_ok = qi < tile.seq_len;
-      __nv_bfloat16* dst = out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + grp) * 128;
+      if (tile.n_chunks == 1) {
+        if (ok) {
+          tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float o[32];
-        tmem_ld32(o_tmem + 32 * c, o);
-        if (row_ok) {
+          for (int h = 0; h < 2; ++h) {
+            if (h >= nh) break;
+            const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
+            __nv_bfloat16* dst =
+                out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + h) * 128 + 64 * half;
+            const uint32_t o_tmem = tmem + 256 * h + lane_off + 128 + 64 * half;
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            st_global_v4(dst + 32 * c + i, pack_bf16x2(o[i] * inv, o[i + 1] * inv),
-                         pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
-                         pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
-                         pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
+            for (int c = 0; c < 2; ++c) {
+              float o[32];
+              tmem_ld32(o_tmem + 32 * c, o);
+              if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                  st_global_v4(dst + 32 * c + i, pack_bf16x2(o[i] * inv, o[i + 1] * inv),
+                               pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
+                               pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
+                               pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
+                }
+              }
+            }
+          }
+        }
+        ok = bar_and(1, kSmThreads, ok);
+        continue;
+      }
+      // ---- a chunk of a split query tile. Chunks count their arrival first; every chunk
+      // but the last stores (max, sum, O) and raises its ready flag, and the last one waits
+      // for those flags, then merges in chunk order with its own O still in tensor memory.
+      // Partial O of a (slot, head) is [32 dim quads][128 rows][4]: a warp's float4 accesses
+      // at one quad cover 512 contiguous bytes. This half owns quads 16*half .. +15.
+      const size_t blk = (size_t)n_q * 128 * 128;    // floats between consecutive slots
+      const size_t ml_stride = (size_t)n_q * 128;
+      int* const cnt = sc.counters + ((size_t)tile.split * groups + u % groups) * kCounterInts;
+      const int nc = tile.n_chunks;
+      ok = bar_and(1, kSmThreads, ok);
+      if (threadIdx.x == 64) *merge_flag = ok ? atomicAdd(cnt, 1) : -1;
+      named_barrier_sync(1, kSmThreads);
+      const int order = *merge_flag;
+      if (order < 0) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      if (order != nc - 1) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h >= nh) break;
+          const size_t hs = (size_t)tile.slot0 * n_q + head0 + h;
+          float* po = sc.part_o + (hs * 128 * 128 + 4 * r) + (size_t)tile.chunk * blk +
+                      (size_t)(16 * half) * 512;
+          const uint32_t o_tmem = tmem + 256 * h + lane_off + 128 + 64 * half;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float o[32];
+            tmem_ld32(o_tmem + 32 * c, o);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(po + (size_t)((32 * c + i) >> 2) * 512) =
+                  make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+          }
+          if (half == 0)
+            sc.part_ml[hs * 128 + r + (size_t)tile.chunk * ml_stride] = make_float2(m[h], L[h]);
+        }
+        __threadfence();
+        named_barrier_sync(1, kSmThreads);
+        if (threadIdx.x == 64) st_release_gpu(cnt + 1 + tile.chunk, 1);
+        ok = bar_and(1, kSmThreads, ok);
+        continue;
+      }
+      // the last chunk: wait (bounded) for the other chunks' partials
+      if (threadIdx.x == 64) {
+        bool ready = true;
+        for (int c = 0; c < nc && ready; ++c) {
+          if (c == tile.chunk) continue;
+          ready = wait_flag(cnt + 1 + c, err);
+        }
+        if (ready) {   // every flag seen: reset the tile's counters for the next launch
+          for (int c = 0; c < nc; ++c) cnt[1 + c] = 0;
+          cnt[0] = 0;
+        }
+        *merge_flag = ready;
+      }
+      named_barrier_sync(1, kSmThreads);
+      if (*merge_flag) {
+        __threadfence();
+        // chunk order, whichever chunk arrives last: M = max m_c, L = sum 2^(m_c - M) l_c,
+        // O = sum 2^(m_c - M) O_c, this chunk's terms taken from its registers and TMEM
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h >= nh) break;
+          const size_t hs = (size_t)tile.slot0 * n_q + head0 + h;
+          const float2* ml0 = sc.part_ml + hs * 128 + r;
+          const float* po0 = sc.part_o + (hs * 128 * 128 + 4 * r) + (size_t)(16 * half) * 512;
+          float f[kMaxChunks], lc[kMaxChunks];
+          float M = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kMaxChunks; ++c) {
+            float2 v = make_float2(-INFINITY, 0.f);
+            if (c == tile.chunk) v = make_float2(m[h], L[h]);
+            else if (c < nc) v = ld_cg_f2(ml0 + c * ml_stride);
+            f[c] = v.x;
+            lc[c] = v.y;
+            M = fmaxf(M, v.x);
+          }
+          float Lm = 0.f;
+#pragma unroll
+          for (int c = 0; c < kMaxChunks; ++c) {
+            f[c] = (f[c] == -INFINITY) ? 0.f : ex2_mufu(f[c] - M);
+            Lm += f[c] * lc[c];
+          }
+          const float inv = Lm > 0.f ? 1.f / Lm : 0.f;
+          __nv_bfloat16* dst =
+              out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + h) * 128 + 64 * half;
+          const uint32_t o_tmem = tmem + 256 * h + lane_off + 128 + 64 * half;
+#pragma unroll 1
+          for (int cb = 0; cb < 4; ++cb) {   // 16 dims per pass
+            float own[16];
+            tmem_ld16(o_tmem + 16 * cb, own);
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < nc; ++c) {
+              if (c == tile.chunk) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] += f[c] * own[i];
+              } else {
+                const float* po = po0 + (size_t)c * blk + (size_t)(4 * cb) * 512;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float4 v = ld_cg_f4(po + k * 512);
+                  acc[4 * k] += f[c] * v.x;
+                  acc[4 * k + 1] += f[c] * v.y;
+                  acc[4 * k + 2] += f[c] * v.z;
+                  acc[4 * k + 3] += f[c] * v.w;
+                }
+              }
+            }
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 16; i += 8) {
+                st_global_v4(dst + 16 * cb + i, pack_bf16x2(acc[i] * inv, acc[i + 1] * inv),
+                             pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv),
+                             pack_bf16x2(acc[i + 4] * inv, acc[i + 5] * inv),
+                             pack_bf16x2(acc[i + 6] * inv, acc[i + 7] * inv));
+              }
+            }
           }
         }
       }
+      ok = bar_and(1, kSmThreads, ok && *merge_flag);
     }
   }
   __syncthreads();
@@ -340,21 +649,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// One block lists the 128-query tiles of every sequence, ordered by the number of key
-// tiles they visit (largest first, a counting sort) so that the longest CTAs start first.
-// Dynamic shared memory: tile offsets of the sequences [n_seqs + 1], then the histogram.
-__device__ __forceinline__ int tile_work(int q0, int L, int window) {
-  const int hi = min(q0 + 127, L - 1) >> 7;
-  const int lo = window > 0 ? max(0, q0 - window + 1) >> 7 : 0;
-  return hi - lo + 1;
+// Key tiles [lo, hi) visited by the 128-query tile at q0 of a sequence of length L.
+__device__ __forceinline__ void tile_keys(int q0, int L, int window, int* lo, int* hi) {
+  *hi = (min(q0 + 127, L - 1) >> 7) + 1;
+  *lo = window > 0 ? max(0, q0 - window + 1) >> 7 : 0;
 }
 
+// One block lists the work items of every sequence, heaviest first (a counting sort on the
+// number of key tiles), so that the persistent CTAs take the longest items first.
+// A query tile with w > C + kMergeTiles key tiles, C = max(kMinChunk, ceil(total work *
+// groups / sms)), is cut into ceil(w / C) (at most kMaxChunks) chunks of near-equal length:
+// only a tile well above the average work per SM is worth a merge. With C at least that
+// average, the split tiles number fewer than sms / groups and their chunks fewer than
+// 2 sms / groups, which bounds the partial buffers.
+// Dynamic shared memory: tile offsets of the sequences [n_seqs + 1], then the histogram.
+struct TileLists {
+  int window[2];
+  AttnTile* tiles[2];
+  int32_t* n_tiles[2];
+};
+
 __global__ void __launch_bounds__(1024)
-    k_attn_tiles(const int32_t* __restrict__ cu, int n_seqs, int window, int max_work,
-                 AttnTile* __restrict__ tiles, int32_t* n_tiles) {
+    k_attn_tiles(const int32_t* __restrict__ cu, int n_seqs, int max_work, int groups, int sms,
+                 TileLists lists, int32_t* zero, int n_zero) {
+  // block b builds list b; block 0 also clears the launches' counters
+  const int window = lists.window[blockIdx.x];
+  AttnTile* __restrict__ tiles = lists.tiles[blockIdx.x];
+  int32_t* n_tiles = lists.n_tiles[blockIdx.x];
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
   extern __shared__ int sh[];
   int* toff = sh;                   // [n_seqs + 1]
   int* hist = sh + n_seqs + 1;      // [max_work + 1]
+  __shared__ unsigned long long wsum;
+  __shared__ int n_split, n_slots, chunk_cap;
   for (int i = threadIdx.x; i <= max_work; i += blockDim.x) hist[i] = 0;
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -363,6 +691,9 @@ __global__ void __launch_bounds__(1024)
       acc += max(0, cu[s + 1] - cu[s] + 127) >> 7;
     }
     toff[n_seqs] = acc;
+    wsum = 0ull;
+    n_split = 0;
+    n_slots = 0;
   }
   __syncthreads();
   const int total = toff[n_seqs];
@@ -375,10 +706,29 @@ __global__ void __launch_bounds__(1024)
     *s_out = lo;
     *q0_out = (g - toff[lo]) * 128;
   };
+  unsigned long long mine = 0;
   for (int g = threadIdx.x; g < total; g += blockDim.x) {
-    int s, q0;
+    int s, q0, lo, hi;
     locate(g, &s, &q0);
-    atomicAdd(&hist[min(tile_work(q0, cu[s + 1] - cu[s], window), max_work)], 1);
+    tile_keys(q0, cu[s + 1] - cu[s], window, &lo, &hi);
+    mine += hi - lo;
+  }
+  atomicAdd(&wsum, mine);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long avg = (wsum * groups + sms - 1) / sms;
+    chunk_cap = static_cast<int>(max(static_cast<unsigned long long>(kMinChunk), avg));
+  }
+  __syncthreads();
+  const int C = chunk_cap;
+  for (int g = threadIdx.x; g < total; g += blockDim.x) {
+    int s, q0, lo, hi;
+    locate(g, &s, &q0);
+    tile_keys(q0, cu[s + 1] - cu[s], window, &lo, &hi);
+    const int w = hi - lo;
+    const int nc = w > C + kMergeTiles ? min((w + C - 1) / C, kMaxChunks) : 1;
+    for (int c = 0; c < nc; ++c)
+      atomicAdd(&hist[min((c + 1) * w / nc - c * w / nc, max_work)], 1);
   }
   __syncthreads();
   if (threadIdx.x == 0) {  // start slot of every work value, largest work first
@@ -388,31 +738,76 @@ __global__ void __launch_bounds__(1024)
       hist[w] = acc;
       acc += c;
     }
-    *n_tiles = total;
+    *n_tiles = acc;
   }
   __syncthreads();
   for (int g = threadIdx.x; g < total; g += blockDim.x) {
-    int s, q0;
+    int s, q0, lo, hi;
     locate(g, &s, &q0);
     const int L = cu[s + 1] - cu[s];
-    const int slot = atomicAdd(&hist[min(tile_work(q0, L, window), max_work)], 1);
-    tiles[slot] = AttnTile{cu[s], L, q0, 0};
+    tile_keys(q0, L, window, &lo, &hi);
+    const int w = hi - lo;
+    const int nc = w > C + kMergeTiles ? min((w + C - 1) / C, kMaxChunks) : 1;
+    int split = -1, slot0 = -1;
+    if (nc > 1) {
+      split = atomicAdd(&n_split, 1);
+      slot0 = atomicAdd(&n_slots, nc);
+    }
+    for (int c = 0; c < nc; ++c) {
+      const int k0 = lo + c * w / nc, k1 = lo + (c + 1) * w / nc;
+      const int slot = atomicAdd(&hist[min(k1 - k0, max_work)], 1);
+      AttnTile t;
+      t.seq_start = cu[s];
+      t.seq_len = L;
+      t.q0 = q0;
+      t.kt0 = k0;
+      t.kt1 = k1;
+      t.chunk = c;
+      t.n_chunks = nc;
+      t.slot0 = slot0;
+      t.split = split;
+      t.pad[0] = t.pad[1] = t.pad[2] = 0;
+      tiles[slot] = t;
+    }
   }
 }
 
 }  // namespace
 
-int attn_max_tiles(int tokens, int n_seqs) { return (tokens + 127) / 128 + n_seqs; }
+int attn_groups(int n_q, int n_kv) {
+  return (n_kv > 0 && ((n_q / n_kv) & 1) == 0) ? n_q / 2 : n_q;
+}
+int attn_split_slots(int groups) { return 2 * num_sms() / groups + 1; }
+int attn_split_tiles(int groups) { return num_sms() / groups + 1; }
+int attn_counter_ints(int groups) { return attn_split_tiles(groups) * groups * kCounterInts; }
+size_t attn_part_ml_pairs(int n_q, int n_kv) {
+  return (size_t)attn_split_slots(attn_groups(n_q, n_kv)) * n_q * 128;
+}
+size_t attn_part_o_floats(int n_q, int n_kv) { return attn_part_ml_pairs(n_q, n_kv) * 128; }
 
-cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int window,
-                            AttnTile* tiles, int32_t* n_tiles, cudaStream_t s) {
+int attn_max_tiles(int tokens, int n_seqs) { return (tokens + 127) / 128 + n_seqs + 2 * num_sms(); }
+
+cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int groups,
+                            int window_a, AttnTile* tiles_a, int32_t* n_tiles_a, int window_b,
+                            AttnTile* tiles_b, int32_t* n_tiles_b, int32_t* zero, int n_zero,
+                            cudaStream_t s) {
   const int max_work = (tokens + 127) / 128 + 1;
   const size_t smem = (size_t)(n_seqs + 1 + max_work + 1) * sizeof(int);
+  if (groups <= 0 || !tiles_a || !n_tiles_a || n_zero < 0) return CC_ERR_INVALID_ARG;
   if (smem > 200 * 1024) return CC_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
     CC_CHECK_CUDA(cudaFuncSetAttribute(k_attn_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem)));
-  k_attn_tiles<<<1, 1024, smem, s>>>(cu_seqlens, n_seqs, window, max_work, tiles, n_tiles);
+  TileLists lists;
+  lists.window[0] = window_a;
+  lists.tiles[0] = tiles_a;
+  lists.n_tiles[0] = n_tiles_a;
+  lists.window[1] = window_b;
+  lists.tiles[1] = tiles_b;
+  lists.n_tiles[1] = n_tiles_b;
+  const int blocks = tiles_b ? 2 : 1;
+  k_attn_tiles<<<blocks, 1024, smem, s>>>(cu_seqlens, n_seqs, max_work, groups, num_sms(), lists,
+                                          zero, n_zero);
   CC_CHECK_CUDA(cudaGetLastError());
   return CC_OK;
 }
@@ -420,7 +815,7 @@ cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, i
 cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               __nv_bfloat16* out, int ld_out, const AttnTile* tiles,
                               const int32_t* n_tiles, int max_tiles, int n_q, int n_kv,
-                              int window, int* err, cudaStream_t s) {
+                              int window, const AttnScratch& sc, int* err, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     CC_CHECK_CUDA(cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -429,11 +824,12 @@ cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
   }
   if (max_tiles <= 0) return CC_OK;
   if (n_kv <= 0 || n_q % n_kv != 0) return CC_ERR_INVALID_ARG;
+  if (!sc.part_o || !sc.part_ml || !sc.counters || !sc.sched) return CC_ERR_INVALID_ARG;
   const float scale_log2 = (1.0f / sqrtf(128.0f)) * kLog2e;
-  const bool paired = ((n_q / n_kv) & 1) == 0;
-  dim3 grid(max_tiles, paired ? n_q / 2 : n_q);
+  const long long items = (long long)max_tiles * attn_groups(n_q, n_kv);
+  const int grid = static_cast<int>(std::min<long long>(items, num_sms()));
   k_attn_prefill<<<grid, kThreads, kSmem, s>>>(tq, tk, tv, out, ld_out, tiles, n_tiles, n_q, n_kv,
-                                               window, scale_log2, err);
+                                               window, scale_log2, sc, err);
   CC_CHECK_CUDA(cudaGetLastError());
   return CC_OK;
 }

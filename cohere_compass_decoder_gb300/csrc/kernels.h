@@ -53,16 +53,51 @@ cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N
 void gemm_choose(int M, int N, int K, int epi, int* bn, int* splits);
 
 // ---------------------------------------------------------------- attention
+// One work item of the prefill attention, for every head group: a 128-query tile and the
+// key tiles [kt0, kt1) it reads. A query tile whose key range is long next to the launch's
+// average work per SM is cut into n_chunks items; each writes a partial (running max, sum,
+// unnormalised O) and the last one to finish merges them.
 struct AttnTile {
   int32_t seq_start;  // first token of the sequence in the packed batch
   int32_t seq_len;
   int32_t q0;         // first query (relative to the sequence) of this 128-row tile
-  int32_t pad;
+  int32_t kt0, kt1;   // key tiles of this item
+  int32_t chunk;      // index among the query tile's n_chunks items
+  int32_t n_chunks;
+  int32_t slot0;      // partial slot of chunk 0 (chunk c uses slot0 + c); -1 when unsplit
+  int32_t split;      // ordinal of the split query tile (its arrival counters); -1 unsplit
+  int32_t pad[3];
 };
 
-// Builds the list of 128-query tiles of all sequences, heaviest first.
-cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int window,
-                            AttnTile* tiles, int32_t* n_tiles, cudaStream_t s);
+// Scratch of one prefill attention launch. `counters` and `sched` must be zero when the
+// launch starts; the kernel leaves the counters at zero and advances `sched`.
+struct AttnScratch {
+  float* part_o = nullptr;      // [slots][n_q][128 rows][128] unnormalised partial outputs
+  float2* part_ml = nullptr;    // [slots][n_q][128 rows] running max (log2 units), sum
+  int32_t* counters = nullptr;  // [split tiles][head groups][1 + max chunks] arrivals, flags
+  int32_t* sched = nullptr;     // next work item (one counter per launch)
+};
+
+// Head groups of a launch: pairs of query heads sharing a KV head, else single heads.
+int attn_groups(int n_q, int n_kv);
+// Capacities of the split bookkeeping for a launch with `groups` head groups (bounds that
+// hold for every cu_seqlens, from the splitting rule of the tile builder).
+int attn_split_slots(int groups);
+int attn_split_tiles(int groups);
+size_t attn_part_o_floats(int n_q, int n_kv);
+size_t attn_part_ml_pairs(int n_q, int n_kv);
+
+// Ints of split bookkeeping (per split tile and head group: an arrival count and one ready
+// flag per chunk) of a launch with `groups` head groups.
+int attn_counter_ints(int groups);
+
+// Builds the work lists of all sequences (query tiles, long ones cut into chunks), heaviest
+// first, for launches with `groups` head groups: list a with window_a and, when tiles_b is
+// not null, list b with window_b, in one launch that also zeroes zero[0 .. n_zero).
+cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int groups,
+                            int window_a, AttnTile* tiles_a, int32_t* n_tiles_a, int window_b,
+                            AttnTile* tiles_b, int32_t* n_tiles_b, int32_t* zero, int n_zero,
+                            cudaStream_t s);
 int attn_max_tiles(int tokens, int n_seqs);
 // Rows (keys) of the K and V boxes the prefill attention kernel loads.
 int attn_kv_box_rows();
@@ -70,7 +105,7 @@ int attn_kv_box_rows();
 cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               __nv_bfloat16* out, int ld_out, const AttnTile* tiles,
                               const int32_t* n_tiles, int max_tiles, int n_q, int n_kv,
-                              int window, int* err, cudaStream_t s);
+                              int window, const AttnScratch& sc, int* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- decode attention
 struct DecodeScratch {
