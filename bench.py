@@ -35,6 +35,13 @@ PREFILL_DESC = ("two-layer pair (sliding+interleaved MRoPE, full NoPE), bf16, ba
                 "seq 2048, hidden 2048, 16/4 heads, head_dim 128, SwiGLU 8192, window 512, "
                 "one 16x16 image at token 300, deepstack [256,2048] after layer 0, tied head "
                 "on the last token, vocab 256000")
+PREFILL_OTHER = {
+    3: ("28-layer stack (full attention at every 4th layer), bf16, batch 1, seq 8192, window "
+        "4096, three 32x32 images, deepstack after layers 0-2, tied head on the last token"),
+    5: ("two-layer pair, varlen packed prefill of 4096/8192/12288/8192 tokens (T = 32768), "
+        "window 4096, 1-4 images per sequence, deepstack after layers 0-1, head on the last "
+        "token of each sequence"),
+}
 DECODE_DESC = ("decode step on the two-layer pair: 64 sequences x 4096 cached bf16 tokens in "
                "16-token pages (permuted page table), window 4096, head on all 64 rows")
 
@@ -51,6 +58,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=0,
                    help="oracle sample: first N tokens of the prefill workload (0: all)")
+    p.add_argument("--prefill-config", type=int, choices=[2, 3, 5], default=2,
+                   help="prefill workload: 2 = two-layer pair T=2048 (the headline), "
+                        "3 = 28-layer stack T=8192, 5 = varlen packed T=32768")
     return p.parse_args()
 
 
@@ -188,7 +198,8 @@ def prefill_leg(args, dist, pk):
     from synth.configs import cfg2
     from cohere_compass_decoder_gb300.workload import GpuWorkload
 
-    inp = Inputs(cfg2())
+    from synth.configs import CONFIGS
+    inp = Inputs(CONFIGS[args.prefill_config]())
     gw = GpuWorkload(inp)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -228,7 +239,8 @@ def prefill_leg(args, dist, pk):
     launches = sum(v["launches_per_step"] for v in kern.values())
     extra = kern.get("row_maps", {}).get("launches_per_step", 0) and 1  # ds map: fill + scatter
     res = dict(ms=ms, value=value, kernels=kern, roofline=roof,
-               launches=int(round((launches + extra) * K)))
+               launches=int(round((launches + extra) * K)), tokens=T,
+               batch=len(inp.wl.seq_lens))
     # e2e through host buffers
     if not args.no_e2e:
         res["e2e"] = prefill_e2e(gw, inp, K, W, dist, stream)
@@ -410,7 +422,9 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": PREFILL_DESC, "global_batch": 1, "seq_len": 2048,
+            "config": {"workload": PREFILL_DESC if args.prefill_config == 2 else
+                       PREFILL_OTHER[args.prefill_config],
+                       "global_batch": pre["batch"], "seq_len": pre["tokens"],
                        "parallelism": "replicas" if dist.world > 1 else "single",
                        "l2": "inputs larger than L2 (1.3 GB of weights per step)"},
             "roofline": pre["roofline"], "cpu_baseline": cpu,
