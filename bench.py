@@ -74,6 +74,36 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
+# ------------------------------------------------------------------------------ traffic
+# DRAM bytes per launch of a kernel from an ncu capture, kept in profiles/traffic.json with a
+# hash of the sources the kernel is built from; reported only while those sources are
+# unchanged since the capture.
+KERNEL_SOURCES = {
+    "gemm_qkv_mlp": ["gemm.cu", "ptx.cuh", "kernels.h", "common.h"],
+    "attn_decode": ["decode.cu", "ptx.cuh", "kernels.h", "common.h"],
+}
+
+
+def sources_sha256(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "cohere_compass_decoder_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("sources_sha256") != sources_sha256(kernel):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 # ------------------------------------------------------------------------------ dist
 class Dist:
     def __init__(self, n):
@@ -220,7 +250,8 @@ def prefill_leg(args, dist, pk):
     flops = 2.0 * T * N1 * s.hidden_size
     ach = flops / (g1["avg_us"] * 1e-6) / 1e12 if g1 else None
     roof = {"kernel": "gemm_qkv_mlp", "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
-            "unit": "TFLOP/s", "frac": (ach / pk["bf16"]) if ach else None, "traffic": None,
+            "unit": "TFLOP/s", "frac": (ach / pk["bf16"]) if ach else None,
+            "traffic": measured_traffic("gemm_qkv_mlp") if args.prefill_config == 2 else None,
             "peak_source": f"{pk['src']} bf16 burst (of {pk['src']})",
             "algorithmic_per_launch": f"2*T*N1*H = {flops:.4g} FLOP"}
     # other classes against their own roofs
@@ -323,7 +354,8 @@ def decode_leg(args, dist, pk):
     per_launch = kv_bytes / len(s.layer_types)
     ach = per_launch / (ad["avg_us"] * 1e-6) / 1e9 if ad else None
     roof = {"kernel": "attn_decode", "bound": "hbm", "achieved": ach, "peak": pk["hbm"],
-            "unit": "GB/s", "frac": (ach / pk["hbm"]) if ach else None, "traffic": None,
+            "unit": "GB/s", "frac": (ach / pk["hbm"]) if ach else None,
+            "traffic": measured_traffic("attn_decode"),
             "peak_source": f"HBM copy (of {pk['src']})",
             "algorithmic_per_launch": f"K+V of the visible keys, {per_launch:.4g} B"}
     gh = kern.get("gemm_head")
