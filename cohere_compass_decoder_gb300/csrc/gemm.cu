@@ -133,7 +133,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, int n0, i
       }
       if (splits > 1) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) atomicAdd(dst + i, v[i]);
+        for (int i = 0; i < 32; i += 4)
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i), "f"(v[i]),
+                       "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
+                       : "memory");
       } else {
         float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
