@@ -175,11 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                    int ld_out, const AttnTile* __restrict__ tiles, const int32_t* n_tiles_p,
                    int n_q, int n_kv, int window, float scale_log2, AttnScratch sc, int* err) {
+  pdl_trigger();
   const int G = n_q / n_kv;
   const bool paired = (G & 1) == 0;                    // two heads share this KV head
   const int nh = paired ? 2 : 1;
   const int groups = paired ? n_q / 2 : n_q;
-  const int n_items = *n_tiles_p * groups;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
@@ -225,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();   // q, k, v and the work list of the previous kernels are complete from here on
+  const int n_items = *n_tiles_p * groups;
 
   int issued_k = 0, issued_v = 0;
   if (warp == 0) {
@@ -672,6 +674,8 @@ struct TileLists {
 __global__ void __launch_bounds__(1024)
     k_attn_tiles(const int32_t* __restrict__ cu, int n_seqs, int max_work, int groups, int sms,
                  TileLists lists, int32_t* zero, int n_zero) {
+  pdl_trigger();
+  pdl_wait();
   // block b builds list b; block 0 also clears the launches' counters
   const int window = lists.window[blockIdx.x];
   AttnTile* __restrict__ tiles = lists.tiles[blockIdx.x];
@@ -806,9 +810,8 @@ cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, i
   lists.tiles[1] = tiles_b;
   lists.n_tiles[1] = n_tiles_b;
   const int blocks = tiles_b ? 2 : 1;
-  k_attn_tiles<<<blocks, 1024, smem, s>>>(cu_seqlens, n_seqs, max_work, groups, num_sms(), lists,
-                                          zero, n_zero);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_attn_tiles, dim3(blocks), dim3(1024), smem, s, cu_seqlens, n_seqs,
+                          max_work, groups, num_sms(), lists, zero, n_zero));
   return CC_OK;
 }
 
@@ -828,9 +831,8 @@ cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
   const float scale_log2 = (1.0f / sqrtf(128.0f)) * kLog2e;
   const long long items = (long long)max_tiles * attn_groups(n_q, n_kv);
   const int grid = static_cast<int>(std::min<long long>(items, num_sms()));
-  k_attn_prefill<<<grid, kThreads, kSmem, s>>>(tq, tk, tv, out, ld_out, tiles, n_tiles, n_q, n_kv,
-                                               window, scale_log2, sc, err);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_attn_prefill, dim3(grid), dim3(kThreads), kSmem, s, tq, tk, tv, out,
+                          ld_out, tiles, n_tiles, n_q, n_kv, window, scale_log2, sc, err));
   return CC_OK;
 }
 

@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,5 +46,25 @@ int num_sms();
 // Zero fill out of bounds. Returns false on failure (bad alignment or driver error).
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t ld, uint32_t box_rows, uint32_t box_cols);
+
+// Launches a kernel of the path with programmatic stream serialization: its CTAs may start
+// (barrier set-up, tensor-memory allocation) while the previous kernel on the stream
+// finishes; every kernel waits (griddepcontrol.wait) before it touches global memory and
+// lets its successor launch (griddepcontrol.launch_dependents) as soon as it starts.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace cc

@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                   const int32_t* __restrict__ n_keys, int n_kv, int window, int splits,
                   float scale_log2, float* __restrict__ part_o, float* __restrict__ part_ml,
                   int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int n_q = n_kv * G;
   const int n = n_keys[b];
@@ -349,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 __global__ void __launch_bounds__(128)
     k_decode_combine(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                      int splits, int n_q, __nv_bfloat16* __restrict__ out, int ld_out) {
+  pdl_trigger();
+  pdl_wait();
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
   const size_t base = ((size_t)b * n_q + h) * splits;
   float M = -INFINITY;
@@ -380,9 +384,9 @@ cc_status launch_dec(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   }
   const float sl2 = (1.0f / sqrtf(128.0f)) * kLog2e;
   dim3 grid(splits, n_kv, batch);
-  k_attn_decode<G><<<grid, kThreads, kSmem, s>>>(tq, tk, tv, n_pages, pt, max_pages, n_keys, n_kv,
-                                                 window, splits, sl2, scr.part_o, scr.part_ml, err);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_attn_decode<G>, grid, dim3(kThreads), kSmem, s, tq, tk, tv, n_pages, pt,
+                          max_pages, n_keys, n_kv, window, splits, sl2, scr.part_o, scr.part_ml,
+                          err));
   return CC_OK;
 }
 
@@ -424,8 +428,8 @@ cc_status launch_attn_decode(const __nv_bfloat16* q, int ld_q, const __nv_bfloat
     default: return CC_ERR_UNSUPPORTED;
   }
   if (st != CC_OK) return st;
-  k_decode_combine<<<dim3(n_q, batch), 128, 0, s>>>(scr.part_o, scr.part_ml, splits, n_q, out,
-                                                     ld_out);
+  CC_CHECK_CUDA(launch_pdl(k_decode_combine, dim3(n_q, batch), dim3(128), 0, s, scr.part_o,
+                          scr.part_ml, splits, n_q, out, ld_out));
   CC_CHECK_CUDA(cudaGetLastError());
   return CC_OK;
 }

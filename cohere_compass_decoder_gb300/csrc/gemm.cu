@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   int* consumed_slot = reinterpret_cast<int*>(bars + 2 * S + 6);
 
+  pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
   const int m_tiles = (M + kBM - 1) / kBM;
   const int n_tiles = N / BN;
@@ -251,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // the previous kernel's outputs (A, the residual) are complete from here on
 
   int issued = 0;  // producer: loads issued
   if (warp == 0) {
@@ -363,8 +365,8 @@ cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
   const int m_tiles = (M + kBM - 1) / kBM;
   const int units = m_tiles * (N / BN) * splits;
   const int grid = units < num_sms() ? units : num_sms();
-  kern<<<grid, kThreads, C::kSmem, s>>>(ta, tb, M, N, K, splits, ep, err);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmem, s, ta, tb, M, N, K, splits,
+                          ep, err));
   return CC_OK;
 }
 

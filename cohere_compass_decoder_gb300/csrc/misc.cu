@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256)
     k_layernorm(const float* __restrict__ x, const void* __restrict__ gamma,
                 OutT* __restrict__ out, int rows, int H, float eps,
                 const int32_t* __restrict__ row_idx, int gamma_bf16) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -78,15 +80,16 @@ cc_status launch_ln(const float* x, const void* gamma, OutT* out, int rows, int 
   if (H % 128 != 0 || H > 128 * kMaxV4) return CC_ERR_UNSUPPORTED;
   const int nv4 = H / 128;
   const dim3 grid((rows + 7) / 8);
+  cudaError_t e = cudaSuccess;
 #define CC_LN_CASE(N) \
-  case N: k_layernorm<N, OutT><<<grid, 256, 0, s>>>(x, gamma, out, rows, H, eps, row_idx, gamma_bf16); break;
+  case N: e = launch_pdl(k_layernorm<N, OutT>, grid, dim3(256), 0, s, x, gamma, out, rows, H, eps, row_idx, gamma_bf16); break;
   switch (nv4) {
     CC_LN_CASE(1) CC_LN_CASE(2) CC_LN_CASE(3) CC_LN_CASE(4) CC_LN_CASE(6) CC_LN_CASE(8)
     CC_LN_CASE(12) CC_LN_CASE(16) CC_LN_CASE(24) CC_LN_CASE(32)
     default: return CC_ERR_UNSUPPORTED;
   }
 #undef CC_LN_CASE
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(e);
   return CC_OK;
 }
 
@@ -102,6 +105,8 @@ struct InvFreq {
 
 __global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, const InvFreq f,
                               int sec_h, int sec_w, float2* __restrict__ table) {
+  pdl_trigger();
+  pdl_wait();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= T * half) return;
   const int t = idx / half, j = idx - t * half;
@@ -119,12 +124,16 @@ __global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, 
 
 // ---------------------------------------------------------------------- row maps
 __global__ void k_fill_i32(int32_t* p, int n, int32_t v) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
 }
 
 __global__ void k_ds_map(const int32_t* __restrict__ rows, int n_rows, int T,
                          int32_t* __restrict__ map, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= n_rows) return;
   const int t = rows[r];
@@ -138,6 +147,8 @@ __global__ void k_ds_map(const int32_t* __restrict__ rows, int n_rows, int T,
 __global__ void k_kv_slots_prefill(const int32_t* __restrict__ cu, int n_seqs, int T,
                                    const int32_t* __restrict__ pt, int max_pages, int ps,
                                    int n_pages, int32_t* __restrict__ slots, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   int lo = 0, hi = n_seqs;  // sequence s with cu[s] <= t < cu[s+1]
@@ -160,6 +171,8 @@ __global__ void k_kv_slots_decode(const int32_t* __restrict__ seq_lens, int batc
                                   const int32_t* __restrict__ pt, int max_pages, int ps,
                                   int n_pages, int32_t* __restrict__ slots,
                                   int32_t* __restrict__ n_keys, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int pos = seq_lens[b];
@@ -195,19 +208,18 @@ cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double the
   InvFreq f{};
   for (int j = 0; j < half; ++j) f.v[j] = std::pow(theta, -2.0 * j / head_dim);
   const int n = T * half;
-  k_mrope_table<<<(n + 255) / 256, 256, 0, s>>>(pos, T, half, f, section[1], section[2], table);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_mrope_table, dim3((n + 255) / 256), dim3(256), 0, s, pos, T, half, f,
+                            section[1], section[2], table));
   return CC_OK;
 }
 
 cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, int* err,
                         cudaStream_t s) {
   if (T <= 0) return CC_OK;
-  k_fill_i32<<<(T + 255) / 256, 256, 0, s>>>(map, T, -1);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_fill_i32, dim3((T + 255) / 256), dim3(256), 0, s, map, T, -1));
   if (n_rows > 0) {
-    k_ds_map<<<(n_rows + 255) / 256, 256, 0, s>>>(rows, n_rows, T, map, err);
-    CC_CHECK_CUDA(cudaGetLastError());
+    CC_CHECK_CUDA(launch_pdl(k_ds_map, dim3((n_rows + 255) / 256), dim3(256), 0, s, rows, n_rows, T,
+                              map, err));
   }
   return CC_OK;
 }
@@ -216,9 +228,8 @@ cc_status launch_kv_slots_prefill(const int32_t* cu_seqlens, int n_seqs, int T,
                                   const int32_t* page_table, int max_pages, int page_size,
                                   int n_pages, int32_t* slots, int* err, cudaStream_t s) {
   if (T <= 0) return CC_OK;
-  k_kv_slots_prefill<<<(T + 255) / 256, 256, 0, s>>>(cu_seqlens, n_seqs, T, page_table, max_pages,
-                                                     page_size, n_pages, slots, err);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_kv_slots_prefill, dim3((T + 255) / 256), dim3(256), 0, s, cu_seqlens,
+                            n_seqs, T, page_table, max_pages, page_size, n_pages, slots, err));
   return CC_OK;
 }
 
@@ -226,9 +237,8 @@ cc_status launch_kv_slots_decode(const int32_t* seq_lens, int batch, const int32
                                  int max_pages, int page_size, int n_pages, int32_t* slots,
                                  int32_t* n_keys, int* err, cudaStream_t s) {
   if (batch <= 0) return CC_OK;
-  k_kv_slots_decode<<<(batch + 127) / 128, 128, 0, s>>>(seq_lens, batch, page_table, max_pages,
-                                                        page_size, n_pages, slots, n_keys, err);
-  CC_CHECK_CUDA(cudaGetLastError());
+  CC_CHECK_CUDA(launch_pdl(k_kv_slots_decode, dim3((batch + 127) / 128), dim3(128), 0, s, seq_lens,
+                            batch, page_table, max_pages, page_size, n_pages, slots, n_keys, err));
   return CC_OK;
 }
 
