@@ -1,0 +1,62 @@
+"""The N > 1 paths of bench.py on the CPU: two ranks over gloo on 127.0.0.1.
+
+The path shards as independent replicas (no collective on the data path); what the ranks
+share is the barrier and the max-over-ranks reduction of the timed interval, and the
+reference arm, which only rank 0 runs and prints.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.Dist(world)
+    assert d.pg is not None and d.world == world and d.rank == rank
+    d.barrier()
+    # each rank's "elapsed ms"; every rank must see the slowest one
+    got = d.max(10.0 + 5.0 * rank)
+    with open(os.path.join(out_dir, f"r{rank}.txt"), "w") as f:
+        f.write(repr(got))
+    d.close()
+
+
+def test_dist_barrier_and_max_over_two_gloo_ranks(tmp_path):
+    port = _free_port()
+    mp.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    vals = [float((tmp_path / f"r{r}.txt").read_text()) for r in range(2)]
+    assert vals == [15.0, 15.0]
+
+
+def test_reference_arm_under_torchrun_prints_once(tmp_path):
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "0", "--cpu-tokens", "96"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = lines[0]
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["n_gpus"] == 2 and line["steps"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
