@@ -13,6 +13,10 @@ Every function follows the definition on the pages, cited by page and section:
   [Kernel story]    C-Kernel-Engine "Cohere Kernel Story", section 1 (parallel block,
                     3:1 layer split, final_logit_scale footer) and section 3 (outputs
                     rounded to BF16 exactly where the contract says).
+  [mlxcel VLM manual]  mlxcel user guide "Vision-Language Models", "Stage 4: Embedding
+                    Merge".
+  [FreeToken PR 454]   FreeToken pull request "feat(mm): serve image input on the Qwen
+                    families", "How it fits together".
 
 Arithmetic is float64 throughout. With ``mirror_bf16=True`` (bf16 workloads) values are
 rounded to bf16 at exactly the points where the GPU path stores bf16 and nowhere else:
@@ -159,6 +163,38 @@ def rotate_half_split(x):
 def apply_rope(x, cos, sin):
     """x * cos + rotate_half_split(x) * sin; x is [T, heads, d], cos/sin [T, d]."""
     return x * cos[:, None, :] + rotate_half_split(x) * sin[:, None, :]
+
+
+# ----------------------------------------------------------------------------------
+# the step before the path: embedding lookup and image-row merge ([Compass issue] "Text
+# decoder forward": h = embed_tokens(tokens); [mlxcel VLM manual] "Stage 4: Embedding
+# Merge": the projected image features take the rows of the image placeholder tokens;
+# [FreeToken PR 454] "How it fits together", scheduler and engine: the rows arrive as a
+# row list (mm_rows) with the gathered features (mm_embeds), merged by one index copy)
+# ----------------------------------------------------------------------------------
+def embed_merge(token_ids, embed, mm_rows=None, mm_embeds=None):
+    """h[t] = embed[token_ids[t]] for every row, then h[mm_rows[r]] = mm_embeds[r].
+
+    Reading: the row list names distinct rows (an index copy with a repeated row has no
+    single result); a token id outside the vocabulary is an error.
+    """
+    token_ids = np.asarray(token_ids, dtype=np.int64)
+    embed = np.asarray(embed, dtype=np.float64)
+    if token_ids.size and (token_ids.min() < 0 or token_ids.max() >= embed.shape[0]):
+        raise ValueError("token id outside the vocabulary")
+    h = np.empty((token_ids.size, embed.shape[1]), dtype=np.float64)
+    for t, tok in enumerate(token_ids):
+        h[t] = embed[tok]
+    if mm_rows is not None and len(mm_rows):
+        mm_rows = np.asarray(mm_rows, dtype=np.int64)
+        if len(set(mm_rows.tolist())) != mm_rows.size:
+            raise ValueError("repeated image row")
+        if mm_rows.min() < 0 or mm_rows.max() >= token_ids.size:
+            raise ValueError("image row outside the sequence")
+        feats = np.asarray(mm_embeds, dtype=np.float64)
+        for r, row in enumerate(mm_rows):
+            h[row] = feats[r]
+    return h
 
 
 # ----------------------------------------------------------------------------------

@@ -413,3 +413,28 @@ def test_decode_equals_last_row_of_prefill(window):
     out2 = O.decode_step(h[n:n + 1], layers, s, [n], [0], perm[table][None, :],
                          lambda i: pools2[i], page, mirror_bf16=False)
     np.testing.assert_array_equal(out2, out)
+
+
+# ---------------------------------------------------------------- embedding merge
+def test_embed_merge_worked_example():
+    g = read_golden("embed_merge_tiny.txt")
+    embed = np.array([[v, 10 * v, -v] for v in range(4)], dtype=np.float64)
+    h = O.embed_merge(g["tokens"], embed, g["mm_rows"], [g["mm_feat0"], g["mm_feat1"]])
+    for t in range(5):
+        assert h[t].tolist() == [float(x) for x in g[f"h{t}"]]
+
+
+def test_embed_merge_without_images_is_the_lookup_and_rejects_bad_input():
+    rng = np.random.default_rng(7)
+    embed = rng.standard_normal((11, 8))
+    toks = rng.integers(0, 11, size=20)
+    h = O.embed_merge(toks, embed)
+    # each row is some embedding row, the one its token names (checked column by column)
+    for t in range(20):
+        assert np.array_equal(h[t], embed[toks[t]])
+    with pytest.raises(ValueError):
+        O.embed_merge([11], embed)
+    with pytest.raises(ValueError):
+        O.embed_merge([1, 2, 3], embed, [1, 1], np.zeros((2, 8)))
+    with pytest.raises(ValueError):
+        O.embed_merge([1, 2, 3], embed, [3], np.zeros((1, 8)))
