@@ -272,11 +272,64 @@ def prefill_leg(args, dist, pk):
     res = dict(ms=ms, value=value, kernels=kern, roofline=roof,
                launches=int(round((launches + extra) * K)), tokens=T,
                batch=len(inp.wl.seq_lens))
+    if s.dtype == "bf16":
+        res["next_rows"] = {"embed_merge_ln": embed_merge_timing(inp, gw, pk)}
     # e2e through host buffers
     if not args.no_e2e:
         res["e2e"] = prefill_e2e(gw, inp, K, W, dist, stream)
     gw.close()
     return res
+
+
+def embed_merge_timing(inp, gw, pk, iters=20):
+    """The step before the path (embedding lookup + image-row merge fused with layer 0's
+    LayerNorm) through its C-ABI op on the workload's token ids, timed with CUDA events."""
+    import numpy as np
+    import torch
+    import cohere_compass_decoder_gb300._lib as L
+    s = inp.shape
+    T, H, V = inp.wl.total_tokens, s.hidden_size, s.vocab_size
+    tok = torch.from_numpy(inp.token_ids).cuda()
+    rows = torch.from_numpy(inp.mm_rows.astype(np.int32)).cuda()
+    from cohere_compass_decoder_gb300.model import to_device
+    feats = to_device(inp.mm_embeds)
+    R = int(rows.numel())
+    h = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    a = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    st = gw.stack
+
+    def run():
+        L.cc_op_embed_merge(tok, T, st.embed, V, H, rows if R else None, feats if R else None, R,
+                            h, st.ln[0], s.layer_norm_eps, a)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    L.cc_op_sync()
+    op_us = e0.elapsed_time(e1) * 1000.0 / iters
+    # the fused kernel alone, as the token-input prefill launches it (library CUDA events)
+    L.cc_profile_read(st.plan)
+    L.cc_profile_enable(st.plan, True)
+    for _ in range(3):
+        st.prefill_tokens(tok, rows if R else None, feats if R else None, h, gw.pos, gw.cu,
+                          gw.n_seqs, gw.ds_rows, gw.ds_feats)
+    torch.cuda.synchronize()
+    prof = L.cc_profile_read(st.plan)
+    L.cc_profile_enable(st.plan, False)
+    n, ms = prof["embed_merge"]
+    us = 1000.0 * ms / max(n, 1)
+    nbytes = T * H * 2 + T * 4 + R * 4 + H * 2 + T * H * 4 + T * H * 2
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"avg_us": us, "bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm"],
+            "op_us": op_us,
+            "note": "embedding lookup + image-row merge fused with layer 0's LayerNorm; avg_us: "
+                    "the kernel in cc_prefill_forward_tokens; op_us: cc_op_embed_merge (row map "
+                    "and scratch allocation included)"}
 
 
 def attn_flops(inp):
@@ -463,6 +516,8 @@ def main():
             "e2e": pre.get("e2e"), "gpu_launches": pre["launches"], "clocks": clk,
             "kernels": pre["kernels"],
         }
+        if pre.get("next_rows"):
+            line["next_rows"] = pre["next_rows"]
         if dec:
             line["decode"] = {"workload": DECODE_DESC, "value": dec["value"], "unit": "tokens/s",
                               "ms_per_step": dec["ms"] / args.steps, "roofline": dec["roofline"],

@@ -23,10 +23,11 @@ EXPORTS = [
     "cc_prefill_forward", "cc_decode_step", "cc_logits", "cc_sync", "cc_op_layernorm",
     "cc_op_mrope_table", "cc_op_gemm_bf16", "cc_op_attention_prefill",
     "cc_op_attention_decode", "cc_op_sync", "cc_profile_enable", "cc_profile_read",
-    "cc_kernel_class_name", "cc_op_attention_decode_noalloc",
+    "cc_kernel_class_name", "cc_op_attention_decode_noalloc", "cc_prefill_forward_tokens",
+    "cc_op_embed_merge",
 ]
 KERNEL_CLASSES = ["rope_table", "row_maps", "layernorm", "gemm_qkv_mlp", "attn_prefill",
-                  "gemm_out_resid", "attn_decode", "gemm_head", "f32_path"]
+                  "gemm_out_resid", "attn_decode", "gemm_head", "f32_path", "embed_merge"]
 
 
 class CCError(RuntimeError):
@@ -88,10 +89,15 @@ def lib() -> C.CDLL:
             "cc_prefill_forward": (C.c_int, [vp, vp, vp, vp, i32, i32, vp, i32,
                                              C.POINTER(vp), i32, C.POINTER(cc_kv_pool), vp,
                                              i32, vp]),
+            "cc_prefill_forward_tokens": (C.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, vp,
+                                                    i32, C.POINTER(vp), i32,
+                                                    C.POINTER(cc_kv_pool), vp, i32, vp]),
             "cc_decode_step": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, C.POINTER(cc_kv_pool), vp]),
             "cc_logits": (C.c_int, [vp, vp, vp, i32, vp, vp]),
             "cc_sync": (C.c_int, [vp, vp]),
             "cc_op_layernorm": (C.c_int, [vp, vp, vp, i32, i32, C.c_float, vp, vp]),
+            "cc_op_embed_merge": (C.c_int, [vp, i32, vp, i32, i32, vp, vp, i32, vp, vp, C.c_float,
+                                            vp, vp]),
             "cc_op_mrope_table": (C.c_int, [vp, i32, i32, C.c_double, p32, vp, vp]),
             "cc_op_gemm_bf16": (C.c_int, [vp, vp, vp, i32, i32, i32, C.c_float, i32, vp]),
             "cc_op_attention_prefill": (C.c_int, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
@@ -242,6 +248,19 @@ def cc_prefill_forward(plan, hidden, pos_thw, cu_seqlens, n_seqs, total_tokens, 
     _check(st, "cc_prefill_forward")
 
 
+def cc_prefill_forward_tokens(plan, token_ids, mm_rows, mm_embeds, n_mm_rows, hidden, pos_thw,
+                              cu_seqlens, n_seqs, total_tokens, ds_rows=None, n_ds_rows=0,
+                              ds_feats=(), kv=None, page_table=None, max_pages=0, stream=None):
+    feats = (C.c_void_p * max(1, len(ds_feats)))(*[_ptr(t) for t in ds_feats])
+    st = lib().cc_prefill_forward_tokens(plan, _ptr(token_ids), _ptr(mm_rows), _ptr(mm_embeds),
+                                         n_mm_rows, _ptr(hidden), _ptr(pos_thw), _ptr(cu_seqlens),
+                                         n_seqs, total_tokens, _ptr(ds_rows), n_ds_rows, feats,
+                                         len(ds_feats),
+                                         C.byref(kv) if kv is not None else None,
+                                         _ptr(page_table), max_pages, _stream(stream))
+    _check(st, "cc_prefill_forward_tokens")
+
+
 def cc_decode_step(plan, hidden, pos_thw, seq_lens, page_table, max_pages, batch, kv,
                    stream=None):
     st = lib().cc_decode_step(plan, _ptr(hidden), _ptr(pos_thw), _ptr(seq_lens),
@@ -276,6 +295,14 @@ def cc_op_mrope_table(pos, tokens, head_dim, theta, section, table, stream=None)
 def cc_op_gemm_bf16(a, b, c, m, n, k, alpha=1.0, accumulate=0, stream=None):
     _check(lib().cc_op_gemm_bf16(_ptr(a), _ptr(b), _ptr(c), m, n, k, alpha, accumulate,
                                  _stream(stream)), "cc_op_gemm_bf16")
+
+
+def cc_op_embed_merge(token_ids, tokens, embed, vocab, hidden_size, mm_rows, mm_embeds,
+                      n_mm_rows, hidden, ln_w=None, eps=1e-5, ln_out=None, stream=None):
+    _check(lib().cc_op_embed_merge(_ptr(token_ids), tokens, _ptr(embed), vocab, hidden_size,
+                                   _ptr(mm_rows), _ptr(mm_embeds), n_mm_rows, _ptr(hidden),
+                                   _ptr(ln_w), eps, _ptr(ln_out), _stream(stream)),
+           "cc_op_embed_merge")
 
 
 def cc_op_attention_prefill(q, k, v, out, ld_out, cu_seqlens, n_seqs, tokens, n_q, n_kv, window,

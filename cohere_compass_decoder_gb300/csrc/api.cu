@@ -173,7 +173,8 @@ struct cc_layer_plan {
   __nv_bfloat16 *a = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *a2 = nullptr;
   float *af = nullptr, *yf = nullptr, *qf = nullptr, *kf = nullptr, *vf = nullptr, *a2f = nullptr;
   float2* rope = nullptr;
-  int32_t *ds_map = nullptr, *kv_slot = nullptr, *n_keys = nullptr, *n_tiles = nullptr;
+  int32_t *ds_map = nullptr, *mm_map = nullptr, *kv_slot = nullptr, *n_keys = nullptr,
+          *n_tiles = nullptr;
   AttnTile *tiles_s = nullptr, *tiles_f = nullptr;
   int max_tiles = 0;
   // prefill attention: partials of split query tiles, then [arrival counters | one item
@@ -307,6 +308,7 @@ extern "C" cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_l
   parts.push_back({reinterpret_cast<void**>(&p->err), 256});
   parts.push_back({reinterpret_cast<void**>(&p->rope), T * (p->d / 2) * sizeof(float2)});
   parts.push_back({reinterpret_cast<void**>(&p->ds_map), T * 4});
+  parts.push_back({reinterpret_cast<void**>(&p->mm_map), T * 4});
   parts.push_back({reinterpret_cast<void**>(&p->kv_slot), T * 4});
   parts.push_back({reinterpret_cast<void**>(&p->n_keys), T * 4});
   parts.push_back({reinterpret_cast<void**>(&p->n_tiles), 256});
@@ -391,12 +393,30 @@ static cc_status plan_gemm(const CUtensorMap& ta, const CUtensorMap& b128, const
   return launch_gemm(ta, bn == 256 ? b256 : b128, M, N, K, bn, splits, epi, ep, err, s);
 }
 
+// Token-id input of the prefill: the embedding merge fused with layer 0's LayerNorm.
+struct EmbedIn {
+  const int32_t* tok;
+  const int32_t* mm_rows;
+  const __nv_bfloat16* mm_embeds;
+  int n_mm_rows;
+};
+
 static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* pos,
                               const int32_t* cu, int n_seqs, int T, const int32_t* ds_rows,
                               int n_ds_rows, const void* const* ds_feats, int n_ds,
                               const cc_kv_pool* kv, const int32_t* page_table, int max_pages,
-                              cudaStream_t s) {
+                              cudaStream_t s, const EmbedIn* emb = nullptr) {
   const cc_model_config& c = p->cfg;
+  if (emb) {
+    // h = embed[tok] with the image rows replaced, and layer 0's a = LayerNorm(h), in one pass
+    if (emb->n_mm_rows > 0)
+      CC_TIMED(p, CC_K_ROW_MAPS, s, launch_ds_map(emb->mm_rows, emb->n_mm_rows, T, p->mm_map, p->err, s));
+    CC_TIMED(p, CC_K_EMBED_MERGE, s,
+             launch_embed_ln(emb->tok, static_cast<const __nv_bfloat16*>(p->embed), p->V,
+                             emb->n_mm_rows > 0 ? p->mm_map : nullptr, emb->mm_embeds, T, p->H,
+                             hidden, static_cast<const __nv_bfloat16*>(p->layers[0].ln_w),
+                             c.layer_norm_eps, p->a, p->err, s));
+  }
   CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos, T, p->d, c.rope_theta, c.mrope_section, p->rope, s));
   if (n_ds > 0) CC_TIMED(p, CC_K_ROW_MAPS, s, launch_ds_map(ds_rows, n_ds_rows, T, p->ds_map, p->err, s));
   if (kv)
@@ -418,8 +438,9 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
   const int tiles = attn_max_tiles(T, n_seqs);
   for (int i = 0; i < c.num_layers; ++i) {
     const bool sliding = p->types[i] == CC_SLIDING;
-    CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(p->layers[i].ln_w),
-                                          p->a, T, p->H, c.layer_norm_eps, nullptr, s));
+    if (!(emb && i == 0))   // with token input, layer 0's LayerNorm ran with the merge
+      CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(p->layers[i].ln_w),
+                                            p->a, T, p->H, c.layer_norm_eps, nullptr, s));
     EpiParams e1;
     e1.q_cols = p->q_cols;
     e1.kv_cols = p->kv_cols;
@@ -518,6 +539,38 @@ extern "C" cc_status cc_prefill_forward(cc_layer_plan* p, float* hidden, const i
                         ds_feats, n_ds, kv, page_table, max_pages, s);
   return prefill_f32(p, hidden, pos_thw, cu_seqlens, n_seqs, total_tokens, ds_rows, n_ds_rows,
                      ds_feats, n_ds, s);
+}
+
+extern "C" cc_status cc_prefill_forward_tokens(
+    cc_layer_plan* p, const int32_t* token_ids, const int32_t* mm_rows, const void* mm_embeds,
+    int32_t n_mm_rows, float* hidden, const int32_t* pos_thw, const int32_t* cu_seqlens,
+    int32_t n_seqs, int32_t total_tokens, const int32_t* ds_rows, int32_t n_ds_rows,
+    const void* const* ds_feats, int32_t n_deepstack, const cc_kv_pool* kv,
+    const int32_t* page_table, int32_t max_pages, void* stream) {
+  if (!p) return CC_ERR_INVALID_ARG;
+  if (!p->bf16) return CC_ERR_UNSUPPORTED;
+  if (total_tokens < 0 || total_tokens > p->T_max || n_seqs < 1 || n_deepstack < 0 ||
+      n_deepstack > p->cfg.num_layers || n_ds_rows < 0 || n_mm_rows < 0)
+    return CC_ERR_INVALID_ARG;
+  if (total_tokens == 0) return CC_OK;
+  if (!token_ids || !hidden || !pos_thw || !cu_seqlens) return CC_ERR_INVALID_ARG;
+  if (n_mm_rows > 0 && (!mm_rows || !mm_embeds)) return CC_ERR_INVALID_ARG;
+  if (n_deepstack > 0 && n_ds_rows > 0) {
+    if (!ds_rows || !ds_feats) return CC_ERR_INVALID_ARG;
+    for (int i = 0; i < n_deepstack; ++i)
+      if (!ds_feats[i]) return CC_ERR_INVALID_ARG;
+  }
+  if (kv) {
+    if (!kv->k || !kv->v || kv->n_pages <= 0 || !page_table || max_pages <= 0)
+      return CC_ERR_INVALID_ARG;
+    for (int i = 0; i < p->cfg.num_layers; ++i)
+      if (!kv->k[i] || !kv->v[i]) return CC_ERR_INVALID_ARG;
+  }
+  const EmbedIn emb{token_ids, mm_rows, static_cast<const __nv_bfloat16*>(mm_embeds), n_mm_rows};
+  const int n_ds = n_ds_rows > 0 ? n_deepstack : 0;
+  return prefill_bf16(p, hidden, pos_thw, cu_seqlens, n_seqs, total_tokens, ds_rows, n_ds_rows,
+                      ds_feats, n_ds, kv, page_table, max_pages, static_cast<cudaStream_t>(stream),
+                      &emb);
 }
 
 extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32_t* pos_thw,
@@ -637,6 +690,30 @@ extern "C" cc_status cc_op_layernorm(const float* x, const void* gamma, void* ou
   return launch_layernorm_bf16(x, static_cast<const __nv_bfloat16*>(gamma),
                                static_cast<__nv_bfloat16*>(out), rows, hidden, eps, row_idx,
                                static_cast<cudaStream_t>(stream));
+}
+
+extern "C" cc_status cc_op_embed_merge(const int32_t* token_ids, int32_t tokens,
+                                       const void* embed, int32_t vocab, int32_t hidden_size,
+                                       const int32_t* mm_rows, const void* mm_embeds,
+                                       int32_t n_mm_rows, float* hidden, const void* ln_w,
+                                       float eps, void* ln_out, void* stream) {
+  if (tokens < 0 || vocab <= 0 || hidden_size <= 0 || n_mm_rows < 0) return CC_ERR_INVALID_ARG;
+  if (tokens == 0) return CC_OK;
+  if (!token_ids || !embed || !hidden || (n_mm_rows > 0 && (!mm_rows || !mm_embeds)) ||
+      (ln_w != nullptr) != (ln_out != nullptr))
+    return CC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* map = nullptr;
+  if (n_mm_rows > 0) CC_CHECK_CUDA(cudaMallocAsync(&map, (size_t)tokens * 4, s));
+  cc_status st = CC_OK;
+  if (map) st = launch_ds_map(mm_rows, n_mm_rows, tokens, map, op_error_flag(), s);
+  if (st == CC_OK)
+    st = launch_embed_ln(token_ids, static_cast<const __nv_bfloat16*>(embed), vocab, map,
+                         static_cast<const __nv_bfloat16*>(mm_embeds), tokens, hidden_size, hidden,
+                         static_cast<const __nv_bfloat16*>(ln_w), eps,
+                         static_cast<__nv_bfloat16*>(ln_out), op_error_flag(), s);
+  if (map) CC_CHECK_CUDA(cudaFreeAsync(map, s));
+  return st;
 }
 
 extern "C" cc_status cc_op_mrope_table(const int32_t* pos, int32_t tokens, int32_t head_dim,
@@ -770,6 +847,6 @@ extern "C" cc_status cc_profile_read(cc_layer_plan* p, cc_kernel_time* out) {
 extern "C" const char* cc_kernel_class_name(int32_t k) {
   static const char* names[CC_K_COUNT] = {"rope_table", "row_maps", "layernorm", "gemm_qkv_mlp",
                                           "attn_prefill", "gemm_out_resid", "attn_decode",
-                                          "gemm_head", "f32_path"};
+                                          "gemm_head", "f32_path", "embed_merge"};
   return (k >= 0 && k < CC_K_COUNT) ? names[k] : "unknown";
 }

@@ -128,6 +128,12 @@ cc_status launch_layernorm_f32(const float* x, const float* gamma, float* out, i
                                float eps, const int32_t* row_idx, cudaStream_t s);
 cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double theta,
                              const int32_t section[3], float2* table, cudaStream_t s);
+// h[row] = f32(mm_embeds[mm_map[row]]) when mm_map[row] >= 0, else f32(embed[tok[row]]);
+// ln_out (nullable) = bf16(LayerNorm(h row) * ln_w). Out-of-range token ids set err.
+cc_status launch_embed_ln(const int32_t* tok, const __nv_bfloat16* embed, int V,
+                          const int32_t* mm_map, const __nv_bfloat16* mm_embeds, int rows, int H,
+                          float* h, const __nv_bfloat16* ln_w, float eps, __nv_bfloat16* ln_out,
+                          int* err, cudaStream_t s);
 cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, int* err,
                         cudaStream_t s);
 // kv_slot for prefill tokens: page_table[seq, t / ps] * ps + t % ps

@@ -15,25 +15,16 @@ namespace {
 // registers (H / 128 float4 per lane, H <= 128 * kMaxV4).
 constexpr int kMaxV4 = 32;  // H <= 4096 in the register-resident variant
 
+// LayerNorm of one row held by a warp (lane owns columns 4 (lane + 32 i) .. +3, i < NV4):
+// mean, then the centred second moment, both reduced across the warp; out = (v - mean) *
+// rstd * gamma.
 template <int NV4, typename OutT>
-__global__ void __launch_bounds__(256)
-    k_layernorm(const float* __restrict__ x, const void* __restrict__ gamma,
-                OutT* __restrict__ out, int rows, int H, float eps,
-                const int32_t* __restrict__ row_idx, int gamma_bf16) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const int src = row_idx ? row_idx[row] : row;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * H);
-  float4 v[NV4];
+__device__ __forceinline__ void ln_row(const float4 (&v)[NV4], const void* __restrict__ gamma,
+                                       int gamma_bf16, int H, float eps, OutT* __restrict__ out_row,
+                                       int lane) {
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV4; ++i) {
-    v[i] = xr[lane + 32 * i];
-    s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-  }
+  for (int i = 0; i < NV4; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const float mean = s / H;
@@ -65,12 +56,74 @@ __global__ void __launch_bounds__(256)
       uint2 pk;
       pk.x = pack_bf16x2(y0, y1);
       pk.y = pack_bf16x2(y2, y3);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (size_t)row * H + c0) = pk;
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out_row) + c0) = pk;
     } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)row * H + c0) =
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out_row) + c0) =
           make_float4(y0, y1, y2, y3);
     }
   }
+}
+
+template <int NV4, typename OutT>
+__global__ void __launch_bounds__(256)
+    k_layernorm(const float* __restrict__ x, const void* __restrict__ gamma,
+                OutT* __restrict__ out, int rows, int H, float eps,
+                const int32_t* __restrict__ row_idx, int gamma_bf16) {
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int src = row_idx ? row_idx[row] : row;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * H);
+  float4 v[NV4];
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) v[i] = xr[lane + 32 * i];
+  ln_row<NV4, OutT>(v, gamma, gamma_bf16, H, eps, out + (size_t)row * H, lane);
+}
+
+// ---------------------------------------------------------------------- embedding merge
+// The step before the path (mlxcel issue "Text decoder forward": h = embed_tokens(tokens);
+// mlxcel VLM manual "Stage 4: Embedding Merge"; FreeToken PR 454 "How it fits together":
+// the image rows take the gathered features, mm_rows -> mm_embeds, by one index copy),
+// fused with the first LayerNorm: one warp per row reads the bf16 source row (the image
+// feature when mm_map[row] >= 0, else the token's embedding row), writes it to h in f32 and,
+// when ln_out is not null, writes LayerNorm(h row) with the same arithmetic as k_layernorm.
+template <int NV4>
+__global__ void __launch_bounds__(256)
+    k_embed_ln(const int32_t* __restrict__ tok, const __nv_bfloat16* __restrict__ embed, int V,
+               const int32_t* __restrict__ mm_map, const __nv_bfloat16* __restrict__ mm_embeds,
+               int rows, int H, float* __restrict__ h, const __nv_bfloat16* __restrict__ ln_w,
+               float eps, __nv_bfloat16* __restrict__ ln_out, int* err) {
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int f = mm_map ? mm_map[row] : -1;
+  const __nv_bfloat16* src = nullptr;
+  if (f >= 0) {
+    src = mm_embeds + (size_t)f * H;
+  } else {
+    const int t = tok[row];
+    if (t >= 0 && t < V) src = embed + (size_t)t * H;
+    else if (lane == 0) set_error(err, CC_DEV_CHECK);   // the row becomes zeros
+  }
+  float4 v[NV4];
+#pragma unroll
+  for (int i = 0; i < NV4; ++i) {
+    const int c0 = 4 * (lane + 32 * i);
+    if (src) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(src + c0);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      v[i] = make_float4(a.x, a.y, b.x, b.y);
+    } else {
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    *reinterpret_cast<float4*>(h + (size_t)row * H + c0) = v[i];
+  }
+  if (ln_out) ln_row<NV4, __nv_bfloat16>(v, ln_w, 1, H, eps, ln_out + (size_t)row * H, lane);
 }
 
 template <typename OutT>
@@ -144,6 +197,21 @@ __global__ void k_ds_map(const int32_t* __restrict__ rows, int n_rows, int T,
   map[t] = r;
 }
 
+// Both steps in one block when the map is short: -1 everywhere, then the row entries.
+__global__ void __launch_bounds__(1024)
+    k_row_map_1blk(const int32_t* __restrict__ rows, int n_rows, int T,
+                   int32_t* __restrict__ map, int* err) {
+  pdl_trigger();
+  pdl_wait();
+  for (int t = threadIdx.x; t < T; t += blockDim.x) map[t] = -1;
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_rows; r += blockDim.x) {
+    const int t = rows[r];
+    if (t < 0 || t >= T) set_error(err, CC_DEV_CHECK);
+    else map[t] = r;
+  }
+}
+
 __global__ void k_kv_slots_prefill(const int32_t* __restrict__ cu, int n_seqs, int T,
                                    const int32_t* __restrict__ pt, int max_pages, int ps,
                                    int n_pages, int32_t* __restrict__ slots, int* err) {
@@ -200,6 +268,29 @@ cc_status launch_layernorm_f32(const float* x, const float* gamma, float* out, i
   return launch_ln<float>(x, gamma, out, rows, H, eps, row_idx, 0, s);
 }
 
+cc_status launch_embed_ln(const int32_t* tok, const __nv_bfloat16* embed, int V,
+                          const int32_t* mm_map, const __nv_bfloat16* mm_embeds, int rows, int H,
+                          float* h, const __nv_bfloat16* ln_w, float eps, __nv_bfloat16* ln_out,
+                          int* err, cudaStream_t s) {
+  if (rows <= 0) return CC_OK;
+  if (H % 128 != 0 || H > 128 * kMaxV4) return CC_ERR_UNSUPPORTED;
+  const dim3 grid((rows + 7) / 8);
+  cudaError_t e = cudaSuccess;
+#define CC_EMB_CASE(N)                                                                     \
+  case N:                                                                                  \
+    e = launch_pdl(k_embed_ln<N>, grid, dim3(256), 0, s, tok, embed, V, mm_map, mm_embeds, \
+                   rows, H, h, ln_w, eps, ln_out, err);                                    \
+    break;
+  switch (H / 128) {
+    CC_EMB_CASE(1) CC_EMB_CASE(2) CC_EMB_CASE(3) CC_EMB_CASE(4) CC_EMB_CASE(6) CC_EMB_CASE(8)
+    CC_EMB_CASE(12) CC_EMB_CASE(16) CC_EMB_CASE(24) CC_EMB_CASE(32)
+    default: return CC_ERR_UNSUPPORTED;
+  }
+#undef CC_EMB_CASE
+  CC_CHECK_CUDA(e);
+  return CC_OK;
+}
+
 cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double theta,
                              const int32_t section[3], float2* table, cudaStream_t s) {
   if (T <= 0) return CC_OK;
@@ -216,6 +307,10 @@ cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double the
 cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, int* err,
                         cudaStream_t s) {
   if (T <= 0) return CC_OK;
+  if (T <= 65536) {
+    CC_CHECK_CUDA(launch_pdl(k_row_map_1blk, dim3(1), dim3(1024), 0, s, rows, n_rows, T, map, err));
+    return CC_OK;
+  }
   CC_CHECK_CUDA(launch_pdl(k_fill_i32, dim3((T + 255) / 256), dim3(256), 0, s, map, T, -1));
   if (n_rows > 0) {
     CC_CHECK_CUDA(launch_pdl(k_ds_map, dim3((n_rows + 255) / 256), dim3(256), 0, s, rows, n_rows, T,

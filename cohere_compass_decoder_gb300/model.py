@@ -58,6 +58,15 @@ class DecoderStack:
         L.cc_prefill_forward(self.plan, hidden, pos, cu_seqlens, n_seqs, hidden.shape[0], ds_rows,
                              n_ds_rows, list(ds_feats), kv, page_table, max_pages, stream)
 
+    def prefill_tokens(self, token_ids, mm_rows, mm_embeds, hidden, pos, cu_seqlens, n_seqs,
+                       ds_rows=None, ds_feats=(), kv=None, page_table=None, max_pages=0,
+                       stream=None):
+        n_mm = 0 if mm_rows is None else int(mm_rows.numel())
+        n_ds_rows = 0 if ds_rows is None else int(ds_rows.numel())
+        L.cc_prefill_forward_tokens(self.plan, token_ids, mm_rows, mm_embeds, n_mm, hidden, pos,
+                                    cu_seqlens, n_seqs, hidden.shape[0], ds_rows, n_ds_rows,
+                                    list(ds_feats), kv, page_table, max_pages, stream)
+
     def decode(self, hidden, pos, seq_lens, page_table, max_pages, kv, stream=None):
         L.cc_decode_step(self.plan, hidden, pos, seq_lens, page_table, max_pages, hidden.shape[0],
                          kv, stream)

@@ -169,6 +169,26 @@ cc_status cc_prefill_forward(cc_layer_plan* plan, float* hidden, const int32_t* 
                              const cc_kv_pool* kv, const int32_t* page_table,
                              int32_t max_pages, void* stream);
 
+/* The step before the path fused with it: cc_prefill_forward starting from token ids.
+ * The embedding merge (Compass issue, "Text decoder forward": h = embed_tokens(tokens);
+ * mlxcel VLM manual "Stage 4: Embedding Merge" and FreeToken PR 454 "How it fits together":
+ * the image placeholder rows take the projected vision features, given as a row list and
+ * the gathered features) runs in one kernel with layer 0's LayerNorm, then the stack runs
+ * as in cc_prefill_forward.
+ *  token_ids int32 [T] in [0, vocab) (device); mm_rows int32 [n_mm_rows] distinct rows in
+ *  [0, T) and mm_embeds bf16 [n_mm_rows, H] (both NULL when n_mm_rows == 0); hidden f32
+ *  [T, H] receives h (it is not read). The other arguments are those of cc_prefill_forward.
+ * bf16 plans only (CC_ERR_UNSUPPORTED otherwise). A token id outside the vocabulary or an
+ * image row outside [0, T) sets the device error flag (cc_sync); that row's h is zero. */
+cc_status cc_prefill_forward_tokens(cc_layer_plan* plan, const int32_t* token_ids,
+                                    const int32_t* mm_rows, const void* mm_embeds,
+                                    int32_t n_mm_rows, float* hidden, const int32_t* pos_thw,
+                                    const int32_t* cu_seqlens, int32_t n_seqs,
+                                    int32_t total_tokens, const int32_t* ds_rows,
+                                    int32_t n_ds_rows, const void* const* ds_feats,
+                                    int32_t n_deepstack, const cc_kv_pool* kv,
+                                    const int32_t* page_table, int32_t max_pages, void* stream);
+
 /* One decode step: one new token per sequence.
  *  hidden    f32 [batch, H] (in: the new tokens' embeddings; out: final h)
  *  pos_thw   int32 [3, batch] (cc_build_decode_positions)
@@ -207,7 +227,8 @@ typedef enum {
   CC_K_ATTN_DECODE = 6,    /* paged decode attention + split combine                 */
   CC_K_GEMM_HEAD = 7,      /* tied head x logit_scale                                */
   CC_K_F32_PATH = 8,       /* kernels of the fp32 variant                            */
-  CC_K_COUNT = 9
+  CC_K_EMBED_MERGE = 9,    /* embedding lookup + image rows + layer 0 LayerNorm      */
+  CC_K_COUNT = 10
 } cc_kernel_class;
 
 typedef struct {
@@ -224,6 +245,18 @@ const char* cc_kernel_class_name(int32_t kernel_class);
  * The steps of the path as separate calls, for composition and testing. They use a
  * library-wide device error flag read by cc_op_sync. Scratch memory they need is
  * taken with cudaMallocAsync/cudaFreeAsync on `stream`. */
+
+/* Embedding merge, optionally fused with a LayerNorm (see cc_prefill_forward_tokens):
+ * hidden[t] = f32(embed[token_ids[t]]), then hidden[mm_rows[r]] = f32(mm_embeds[r]); when
+ * ln_w is not NULL also ln_out[t] = bf16(LayerNorm(hidden[t]) * ln_w) with the arithmetic
+ * of cc_op_layernorm. token_ids int32 [T]; embed bf16 [vocab, H]; mm_rows int32 [R]
+ * distinct (which of two equal rows wins is unspecified); mm_embeds bf16 [R, H]; hidden
+ * f32 [T, H]; ln_w bf16 [H]; ln_out bf16 [T, H]. H % 128 == 0, H <= 4096. Bad indices set the
+ * op error flag (cc_op_sync). */
+cc_status cc_op_embed_merge(const int32_t* token_ids, int32_t tokens, const void* embed,
+                            int32_t vocab, int32_t hidden_size, const int32_t* mm_rows,
+                            const void* mm_embeds, int32_t n_mm_rows, float* hidden,
+                            const void* ln_w, float eps, void* ln_out, void* stream);
 
 /* LayerNorm (Compass issue, "Text decoder forward": weight only, no bias, f32 statistics,
  * biased variance, eps inside the square root): out[r] = bf16(gamma * (x[src] - mean) /

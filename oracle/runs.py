@@ -10,8 +10,9 @@ import numpy as np
 from . import decoder as O
 
 
-def run_prefill(inp, mirror_bf16=None, return_all=False):
-    """Final residual stream h [T, H] and logits of the head rows, both float64."""
+def run_prefill(inp, mirror_bf16=None, return_all=False, hidden=None):
+    """Final residual stream h [T, H] and logits of the head rows, both float64 (``hidden``:
+    the stack's input instead of the workload's hidden states)."""
     wl = inp.wl
     shape = O.shape_dict(inp.shape)
     if mirror_bf16 is None:
@@ -19,7 +20,8 @@ def run_prefill(inp, mirror_bf16=None, return_all=False):
     spans = [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w) for i in inp.images]
     pos, _ = O.positions(wl.seq_lens, spans)
     ds = [inp.ds(i) for i in range(wl.n_deepstack)]
-    out = O.prefill(inp.hidden, inp.layer, shape, pos, inp.cu_seqlens, inp.ds_rows, ds,
+    out = O.prefill(inp.hidden if hidden is None else hidden, inp.layer, shape, pos,
+                    inp.cu_seqlens, inp.ds_rows, ds,
                     mirror_bf16, return_all=return_all)
     h, hs = (out if return_all else (out, None))
     logits = O.logits(h[inp.head_rows], inp.final_ln, inp.embed, shape, mirror_bf16)

@@ -143,6 +143,31 @@ class Inputs:
             self._ds[key] = _draw(rng, (R, self.shape.hidden_size), 0.1, 0.0, self.bf16)
         return self._ds[key]
 
+    # ---- token-id input (the embedding merge before the path) ----------------------------
+    @property
+    def token_ids(self) -> np.ndarray:
+        """int32 [T], uniform over the vocabulary (placeholder ids at image rows are
+        irrelevant: those rows take the image features)."""
+        if "tok" not in self._ds:
+            rng = np.random.default_rng((self.wl.seed, 7))
+            self._ds["tok"] = rng.integers(0, self.shape.vocab_size, size=self.wl.total_tokens,
+                                           dtype=np.int64).astype(np.int32)
+        return self._ds["tok"]
+
+    @property
+    def mm_rows(self) -> np.ndarray:
+        """The image rows (those of every image span), in order."""
+        return self.ds_rows
+
+    @property
+    def mm_embeds(self) -> np.ndarray:
+        """Projected vision features of the image rows, N(0, 1) (bf16 workloads: bf16)."""
+        if "mm" not in self._ds:
+            rng = np.random.default_rng((self.wl.seed, 8))
+            self._ds["mm"] = _draw(rng, (len(self.mm_rows), self.shape.hidden_size), 1.0, 0.0,
+                                   self.bf16)
+        return self._ds["mm"]
+
     # ---- decode state ------------------------------------------------------------------
     @property
     def max_pages(self) -> int:

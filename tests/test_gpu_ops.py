@@ -45,6 +45,45 @@ def test_layernorm_matches_oracle(rows, H):
     assert np.mean(got != want) < 0.01
 
 
+# --------------------------------------------------------------------------- embedding merge
+@pytest.mark.parametrize("T,H,V,n_img", [(300, 256, 1000, 37), (1, 128, 7, 0), (513, 2048, 4000, 200)])
+def test_embed_merge_matches_oracle(T, H, V, n_img):
+    rng = np.random.default_rng(T + H)
+    embed = bf16_dev(0.5 * rng.standard_normal((V, H)))
+    tok = rng.integers(0, V, size=T).astype(np.int32)
+    rows = rng.permutation(T)[:n_img].astype(np.int32)
+    feats = bf16_dev(rng.standard_normal((max(n_img, 1), H)))[:n_img]
+    g = bf16_dev(1 + 0.02 * rng.standard_normal(H))
+    h = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    a = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    tok_d = torch.from_numpy(tok).cuda()
+    rows_d = torch.from_numpy(rows).cuda() if n_img else None
+    L.cc_op_embed_merge(tok_d, T, embed, V, H, rows_d, feats if n_img else None, n_img, h, g, 1e-5, a)
+    _sync()
+    want = O.embed_merge(tok, f64(embed), rows if n_img else None, f64(feats) if n_img else None)
+    assert np.array_equal(f64(h), want)               # a copy: bit-exact
+    # the fused LayerNorm is the standalone one, bit for bit
+    a2 = torch.empty_like(a)
+    L.cc_op_layernorm(h, g, a2, T, H, 1e-5, None)
+    _sync()
+    assert torch.equal(a, a2)
+    ln_ref = O.round_bf16(O.layer_norm(want, f64(g), 1e-5))
+    assert np.abs(f64(a) - ln_ref).max() <= np.abs(ln_ref).max() * 2.0 ** -7
+
+
+def test_embed_merge_reports_a_token_outside_the_vocabulary():
+    V, H, T = 50, 128, 20
+    embed = torch.zeros(V, H, dtype=torch.bfloat16, device="cuda")
+    tok = torch.arange(T, dtype=torch.int32, device="cuda")
+    tok[5] = V
+    h = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    L.cc_op_embed_merge(tok, T, embed, V, H, None, None, 0, h)
+    with pytest.raises(L.CCError) as e:
+        L.cc_op_sync()
+    assert e.value.status == L.CC_ERR_DEVICE_CHECK
+    assert torch.count_nonzero(h[5]) == 0
+
+
 # --------------------------------------------------------------------------- MRoPE table
 @pytest.mark.parametrize("section,theta", [((24, 20, 20), 50000.0), ((12, 10, 10), 1e4)])
 def test_mrope_table_matches_oracle(section, theta):

@@ -14,6 +14,8 @@ from oracle import runs as R
 from synth import Inputs, Workload, ImageSpan, small_shape, SLIDING, FULL
 from synth.configs import cfg1, cfg2, cfg3, cfg4, cfg5
 from cohere_compass_decoder_gb300.workload import GpuWorkload, as_numpy
+from cohere_compass_decoder_gb300.model import to_device
+import cohere_compass_decoder_gb300._lib as L
 
 from gpu_util import require_gpu, assert_close, err_stats
 
@@ -74,6 +76,33 @@ def test_small_stack_mha_and_no_images():
                  hidden=128, inter=128, vocab=256, seed=23)
     gw, h, lg = _run(inp)
     _check(inp, gw, h, lg)
+
+
+def test_prefill_from_token_ids():
+    """The embedding merge fused with layer 0's LayerNorm gives the same stack output, bit for
+    bit, as the merge op followed by the hidden-state prefill, and the oracle's merge + stack."""
+    inp = _small("small_tok", [300], [ImageSpan(0, 37, 1, 8, 8)], 2, seed=29)
+    gw = GpuWorkload(inp)
+    st = gw.stack
+    s = inp.shape
+    tok = torch.from_numpy(inp.token_ids).cuda()
+    rows = torch.from_numpy(inp.mm_rows.astype(np.int32)).cuda()
+    feats = to_device(inp.mm_embeds)
+    T = inp.wl.total_tokens
+    h1 = torch.empty(T, s.hidden_size, dtype=torch.float32, device="cuda")
+    st.prefill_tokens(tok, rows, feats, h1, gw.pos, gw.cu, gw.n_seqs, gw.ds_rows, gw.ds_feats)
+    h2 = torch.empty_like(h1)
+    L.cc_op_embed_merge(tok, T, st.embed, s.vocab_size, s.hidden_size, rows, feats,
+                        int(rows.numel()), h2)
+    L.cc_op_sync()
+    gw.prefill(h2)
+    gw.sync()
+    assert torch.equal(h1, h2)
+    from oracle import decoder as OD
+    h0 = OD.embed_merge(inp.token_ids, OD.from_storage(inp.embed), inp.mm_rows,
+                        OD.from_storage(inp.mm_embeds))
+    h_ref, _ = R.run_prefill(inp, hidden=h0)
+    assert_close(as_numpy(h1), h_ref, TOL_MAX, TOL_MEAN, "hidden")
 
 
 def test_causal_prefix_on_gpu():
