@@ -274,6 +274,8 @@ def prefill_leg(args, dist, pk):
                batch=len(inp.wl.seq_lens))
     if s.dtype == "bf16":
         res["next_rows"] = {"embed_merge_ln": embed_merge_timing(inp, gw, pk)}
+        if args.prefill_config == 2:
+            res["next_rows"]["chunked_prefill"] = chunked_prefill_timing(inp, gw, pk)
     # e2e through host buffers
     if not args.no_e2e:
         res["e2e"] = prefill_e2e(gw, inp, K, W, dist, stream)
@@ -330,6 +332,64 @@ def embed_merge_timing(inp, gw, pk, iters=20):
             "note": "embedding lookup + image-row merge fused with layer 0's LayerNorm; avg_us: "
                     "the kernel in cc_prefill_forward_tokens; op_us: cc_op_embed_merge (row map "
                     "and scratch allocation included)"}
+
+
+def chunked_prefill_timing(inp, gw, pk, steps=10):
+    """Chunked prefill (the handoff step): the workload's tokens as a second chunk that
+    continues a cached prefix of the same length, attention over the paged cache."""
+    import numpy as np
+    import torch
+    import cohere_compass_decoder_gb300._lib as L
+    s = inp.shape
+    T = inp.wl.total_tokens
+    if len(inp.wl.seq_lens) != 1:
+        return None
+    spans = [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w) for i in inp.images]
+    pos2, _ = L.cc_build_mrope_positions(spans, [2 * T])
+    pos_a = torch.tensor(np.ascontiguousarray(np.asarray(pos2)[:, :T]), dtype=torch.int32,
+                         device="cuda")
+    pos_b = torch.tensor(np.ascontiguousarray(np.asarray(pos2)[:, T:]), dtype=torch.int32,
+                         device="cuda")
+    ps = 16
+    max_pages = (2 * T + ps - 1) // ps
+    table = torch.arange(max_pages, dtype=torch.int32, device="cuda").view(1, -1)
+    kp = [torch.zeros(max_pages, s.num_key_value_heads, ps, s.head_dim, dtype=torch.bfloat16,
+                      device="cuda") for _ in range(s.num_layers)]
+    vp = [torch.zeros_like(t) for t in kp]
+    kv = L.make_kv_pool(kp, vp, max_pages)
+    st = gw.stack
+    cu = gw.cu
+    h = gw.fresh_hidden()
+    L.cc_prefill_forward(st.plan, h, pos_a, cu, 1, T, gw.ds_rows,
+                         0 if gw.ds_rows is None else int(gw.ds_rows.numel()), gw.ds_feats, kv,
+                         table, max_pages)
+    prefix = torch.tensor([T], dtype=torch.int32, device="cuda")
+    pool = [gw.fresh_hidden() for _ in range(steps + 3)]
+
+    def run(i):
+        L.cc_prefill_forward_chunk(st.plan, pool[i], pos_b, cu, 1, T, prefix, kv, table,
+                                   max_pages)
+    for i in range(3):
+        run(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        run(3 + i)
+    e1.record()
+    torch.cuda.synchronize()
+    L.cc_sync(st.plan)
+    ms = e0.elapsed_time(e1) / steps
+    # attention of the chunk: query T + i sees T + i + 1 keys (full) or min(., window)
+    i = np.arange(T, 2 * T)
+    vis = 0
+    for lt in s.layer_types:
+        vis += int((i + 1).sum() if lt != "sliding_attention" else np.minimum(i + 1, s.sliding_window).sum())
+    flops = 4.0 * s.head_dim * s.num_attention_heads * vis
+    return {"chunk_tokens": T, "prefix_tokens": T, "ms_per_chunk": ms,
+            "tokens_per_s": T / (ms / 1e3), "attn_gflop_per_chunk": flops / 1e9,
+            "note": "cc_prefill_forward_chunk: the layer stack over a 2048-token chunk that "
+                    "continues a 2048-token prefix in the paged cache (no head)"}
 
 
 def attn_flops(inp):

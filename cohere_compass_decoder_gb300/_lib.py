@@ -24,7 +24,7 @@ EXPORTS = [
     "cc_op_mrope_table", "cc_op_gemm_bf16", "cc_op_attention_prefill",
     "cc_op_attention_decode", "cc_op_sync", "cc_profile_enable", "cc_profile_read",
     "cc_kernel_class_name", "cc_op_attention_decode_noalloc", "cc_prefill_forward_tokens",
-    "cc_op_embed_merge",
+    "cc_op_embed_merge", "cc_prefill_forward_chunk",
 ]
 KERNEL_CLASSES = ["rope_table", "row_maps", "layernorm", "gemm_qkv_mlp", "attn_prefill",
                   "gemm_out_resid", "attn_decode", "gemm_head", "f32_path", "embed_merge"]
@@ -92,6 +92,9 @@ def lib() -> C.CDLL:
             "cc_prefill_forward_tokens": (C.c_int, [vp, vp, vp, vp, i32, vp, vp, vp, i32, i32, vp,
                                                     i32, C.POINTER(vp), i32,
                                                     C.POINTER(cc_kv_pool), vp, i32, vp]),
+            "cc_prefill_forward_chunk": (C.c_int, [vp, vp, vp, vp, i32, i32, vp, vp, i32,
+                                                   C.POINTER(vp), i32, C.POINTER(cc_kv_pool), vp,
+                                                   i32, vp]),
             "cc_decode_step": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, C.POINTER(cc_kv_pool), vp]),
             "cc_logits": (C.c_int, [vp, vp, vp, i32, vp, vp]),
             "cc_sync": (C.c_int, [vp, vp]),
@@ -259,6 +262,17 @@ def cc_prefill_forward_tokens(plan, token_ids, mm_rows, mm_embeds, n_mm_rows, hi
                                          C.byref(kv) if kv is not None else None,
                                          _ptr(page_table), max_pages, _stream(stream))
     _check(st, "cc_prefill_forward_tokens")
+
+
+def cc_prefill_forward_chunk(plan, hidden, pos_thw, cu_seqlens, n_seqs, total_tokens, prefix_lens,
+                             kv, page_table, max_pages, ds_rows=None, n_ds_rows=0, ds_feats=(),
+                             stream=None):
+    feats = (C.c_void_p * max(1, len(ds_feats)))(*[_ptr(t) for t in ds_feats])
+    st = lib().cc_prefill_forward_chunk(plan, _ptr(hidden), _ptr(pos_thw), _ptr(cu_seqlens), n_seqs,
+                                        total_tokens, _ptr(prefix_lens), _ptr(ds_rows), n_ds_rows,
+                                        feats, len(ds_feats), C.byref(kv), _ptr(page_table),
+                                        max_pages, _stream(stream))
+    _check(st, "cc_prefill_forward_chunk")
 
 
 def cc_decode_step(plan, hidden, pos_thw, seq_lens, page_table, max_pages, batch, kv,

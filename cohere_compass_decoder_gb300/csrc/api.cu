@@ -405,8 +405,12 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
                               const int32_t* cu, int n_seqs, int T, const int32_t* ds_rows,
                               int n_ds_rows, const void* const* ds_feats, int n_ds,
                               const cc_kv_pool* kv, const int32_t* page_table, int max_pages,
-                              cudaStream_t s, const EmbedIn* emb = nullptr) {
+                              cudaStream_t s, const EmbedIn* emb = nullptr,
+                              const int32_t* prefix = nullptr) {
   const cc_model_config& c = p->cfg;
+  // chunked prefill: the tokens continue cached prefixes; attention reads every key from the
+  // paged cache, which the projection epilogue fills with this call's keys first
+  const bool chunked = prefix != nullptr;
   if (emb) {
     // h = embed[tok] with the image rows replaced, and layer 0's a = LayerNorm(h), in one pass
     if (emb->n_mm_rows > 0)
@@ -421,12 +425,13 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
   if (n_ds > 0) CC_TIMED(p, CC_K_ROW_MAPS, s, launch_ds_map(ds_rows, n_ds_rows, T, p->ds_map, p->err, s));
   if (kv)
     CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_prefill(cu, n_seqs, T, page_table, max_pages, c.kv_page_size,
-                                            kv->n_pages, p->kv_slot, p->err, s));
+                                            kv->n_pages, p->kv_slot, p->err, s, prefix));
   // both work lists (sliding, full) in one launch, which also clears the attention counters
   CC_TIMED(p, CC_K_ROW_MAPS, s, launch_attn_tiles(cu, n_seqs, T, p->attn_groups_n, c.sliding_window,
                                                  p->tiles_s, p->n_tiles, 0, p->tiles_f,
                                                  p->n_tiles + 1, p->attn_cnt,
-                                                 static_cast<int>(p->attn_cnt_ints), s));
+                                                 static_cast<int>(p->attn_cnt_ints), s, prefix,
+                                                 chunked ? max_pages * c.kv_page_size : 0));
   const int32_t* layer_sched0 = p->attn_cnt + (p->attn_cnt_ints - c.num_layers);
   CUtensorMap ta, ta2, tq, tk, tv;
   if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, T), p->H, p->H, 128, 64) ||
@@ -466,9 +471,20 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
     sc.part_ml = p->attn_part_ml;
     sc.counters = p->attn_cnt;
     sc.sched = const_cast<int32_t*>(layer_sched0) + i;
-    CC_TIMED(p, CC_K_ATTN_PREFILL, s, launch_attn_prefill(tq, tk, tv, p->a2, p->K2, sliding ? p->tiles_s : p->tiles_f,
+    AttnPaged paged;
+    CUtensorMap pk = tk, pv = tv;
+    if (chunked) {
+      const uint64_t pool_rows = (uint64_t)kv->n_pages * p->nkv * c.kv_page_size;
+      if (!make_tmap_bf16_2d(&pk, kv->k[i], pool_rows, p->d, p->d, 16, 64) ||
+          !make_tmap_bf16_2d(&pv, kv->v[i], pool_rows, p->d, p->d, 16, 64))
+        return CC_ERR_CUDA;
+      paged.pt = page_table;
+      paged.max_pages = max_pages;
+      paged.n_pages = kv->n_pages;
+    }
+    CC_TIMED(p, CC_K_ATTN_PREFILL, s, launch_attn_prefill(tq, pk, pv, p->a2, p->K2, sliding ? p->tiles_s : p->tiles_f,
                                         p->n_tiles + (sliding ? 0 : 1), tiles, p->nq, p->nkv,
-                                        sliding ? c.sliding_window : 0, sc, p->err, s));
+                                        sliding ? c.sliding_window : 0, sc, p->err, s, paged));
     EpiParams e2;
     e2.c = hidden;
     e2.ldc = p->H;
@@ -571,6 +587,34 @@ extern "C" cc_status cc_prefill_forward_tokens(
   return prefill_bf16(p, hidden, pos_thw, cu_seqlens, n_seqs, total_tokens, ds_rows, n_ds_rows,
                       ds_feats, n_ds, kv, page_table, max_pages, static_cast<cudaStream_t>(stream),
                       &emb);
+}
+
+extern "C" cc_status cc_prefill_forward_chunk(
+    cc_layer_plan* p, float* hidden, const int32_t* pos_thw, const int32_t* cu_seqlens,
+    int32_t n_seqs, int32_t total_tokens, const int32_t* prefix_lens, const int32_t* ds_rows,
+    int32_t n_ds_rows, const void* const* ds_feats, int32_t n_deepstack, const cc_kv_pool* kv,
+    const int32_t* page_table, int32_t max_pages, void* stream) {
+  if (!p) return CC_ERR_INVALID_ARG;
+  if (!p->bf16) return CC_ERR_UNSUPPORTED;
+  if (p->cfg.kv_page_size != 16 || p->d != 128) return CC_ERR_UNSUPPORTED;
+  if (total_tokens < 0 || total_tokens > p->T_max || n_seqs < 1 || n_deepstack < 0 ||
+      n_deepstack > p->cfg.num_layers || n_ds_rows < 0)
+    return CC_ERR_INVALID_ARG;
+  if (total_tokens == 0) return CC_OK;
+  if (!hidden || !pos_thw || !cu_seqlens || !prefix_lens || !kv || !page_table || max_pages <= 0)
+    return CC_ERR_INVALID_ARG;
+  if (!kv->k || !kv->v || kv->n_pages <= 0) return CC_ERR_INVALID_ARG;
+  for (int i = 0; i < p->cfg.num_layers; ++i)
+    if (!kv->k[i] || !kv->v[i]) return CC_ERR_INVALID_ARG;
+  if (n_deepstack > 0 && n_ds_rows > 0) {
+    if (!ds_rows || !ds_feats) return CC_ERR_INVALID_ARG;
+    for (int i = 0; i < n_deepstack; ++i)
+      if (!ds_feats[i]) return CC_ERR_INVALID_ARG;
+  }
+  const int n_ds = n_ds_rows > 0 ? n_deepstack : 0;
+  return prefill_bf16(p, hidden, pos_thw, cu_seqlens, n_seqs, total_tokens, ds_rows, n_ds_rows,
+                      ds_feats, n_ds, kv, page_table, max_pages, static_cast<cudaStream_t>(stream),
+                      nullptr, prefix_lens);
 }
 
 extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32_t* pos_thw,

@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_attn_prefill(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                    int ld_out, const AttnTile* __restrict__ tiles, const int32_t* n_tiles_p,
-                   int n_q, int n_kv, int window, float scale_log2, AttnScratch sc, int* err) {
+                   int n_q, int n_kv, int window, float scale_log2, AttnScratch sc, AttnPaged paged,
+                   int* err) {
   pdl_trigger();
   const int G = n_q / n_kv;
   const bool paired = (G & 1) == 0;                    // two heads share this KV head
@@ -254,25 +255,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + kOffQ + h * kTile + kHalf, &tm_q, bar(B_Q), qx + 64,
                       tile.seq_start + tile.q0);
         }
+        // one 128-key tile of K or V: two 64-column boxes of the contiguous K/V, or, paged,
+        // the tile's 8 pages of 16 keys gathered through the page table (a page past the
+        // call's last key is never read by a query: page 0 stands in for it)
+        const int32_t* pt_row =
+            paged.pt ? paged.pt + (size_t)tile.seq * paged.max_pages : nullptr;
+        const int key_end = tile.prefix + tile.seq_len;
+        auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t fb, int kt) {
+          if (!pt_row) {
+            const int y = tile.seq_start + kt * kKeys;
+            tma_load_2d(dst, tm, fb, kx, y);
+            tma_load_2d(dst + kHalf, tm, fb, kx + 64, y);
+            return;
+          }
+          int ids[kKeys / 16];
+#pragma unroll
+          for (int i = 0; i < kKeys / 16; ++i) {
+            const int pg = kt * (kKeys / 16) + i;
+            ids[i] = pg < paged.max_pages ? pt_row[pg] : -1;
+          }
+#pragma unroll
+          for (int i = 0; i < kKeys / 16; ++i) {
+            int id = ids[i];
+            if (id < 0 || id >= paged.n_pages) {
+              if ((kt * (kKeys / 16) + i) * 16 < key_end) set_error(err, CC_DEV_CHECK);
+              id = 0;
+            }
+            const int y = (id * n_kv + head0 / G) * 16;
+            tma_load_2d(dst + i * 2048, tm, fb, 0, y);
+            tma_load_2d(dst + kHalf + i * 2048, tm, fb, 64, y);
+          }
+        };
         // K runs up to one tile ahead of V within the item
         bool ok = true;
         for (int a = 0, b = 0; a < n || b < n;) {
           if (a < n && a <= b + 1) {
             const int st = issued_k % kKStages;
             if (!(ok = mbar_wait(bar(B_KEMPTY + st), ((issued_k / kKStages) & 1) ^ 1, err))) break;
-            const int y = tile.seq_start + (tile.kt0 + a) * kKeys;
             mbar_expect_tx(bar(B_KFULL + st), kTile);
-            tma_load_2d(sbase + kOffK + st * kTile, &tm_k, bar(B_KFULL + st), kx, y);
-            tma_load_2d(sbase + kOffK + st * kTile + kHalf, &tm_k, bar(B_KFULL + st), kx + 64, y);
+            load_tile(&tm_k, sbase + kOffK + st * kTile, bar(B_KFULL + st), tile.kt0 + a);
             ++a;
             ++issued_k;
           } else {
             const int st = issued_v % kVStages;
             if (!(ok = mbar_wait(bar(B_VEMPTY + st), ((issued_v / kVStages) & 1) ^ 1, err))) break;
-            const int y = tile.seq_start + (tile.kt0 + b) * kKeys;
             mbar_expect_tx(bar(B_VFULL + st), kTile);
-            tma_load_2d(sbase + kOffV + st * kTile, &tm_v, bar(B_VFULL + st), kx, y);
-            tma_load_2d(sbase + kOffV + st * kTile + kHalf, &tm_v, bar(B_VFULL + st), kx + 64, y);
+            load_tile(&tm_v, sbase + kOffV + st * kTile, bar(B_VFULL + st), tile.kt0 + b);
             ++b;
             ++issued_v;
           }
@@ -371,9 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = tile.kt1 - tile.kt0;
       const int head0 = (u % groups) * nh;
       const int q0 = tile.q0;
-      const int qi = q0 + r;                         // query index in its sequence
+      const int qi = q0 + r;                         // query row among the call's tokens
+      const int qa = tile.prefix + qi;               // its position: the key index it sees up to
       // this warp's rows that lie inside the sequence (rows past its end are never stored)
-      const int qw_lo = q0 + quarter * 32, qw_hi = min(qw_lo + 31, tile.seq_len - 1);
+      const int qw_lo = tile.prefix + q0 + quarter * 32;
+      const int qw_hi = tile.prefix + min(q0 + quarter * 32 + 31, tile.seq_len - 1);
       float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // l: this half's keys
       for (int t = 0; t < n && ok; ++t) {
         const int g = gt + t;
@@ -393,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             tmem_ld64(s_tmem + 64 * half, s);
             if (!full) {
-              const int hi_c = qi - kbase;                           // causal: c <= hi_c
-              const int lo_c = window > 0 ? qi - window + 1 - kbase : -1;
+              const int hi_c = qa - kbase;                           // causal: c <= hi_c
+              const int lo_c = window > 0 ? qa - window + 1 - kbase : -1;
 #pragma unroll
               for (int c = 0; c < 64; ++c) s[c] = (c <= hi_c && c >= lo_c) ? s[c] : -INFINITY;
             }
@@ -651,10 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Key tiles [lo, hi) visited by the 128-query tile at q0 of a sequence of length L.
-__device__ __forceinline__ void tile_keys(int q0, int L, int window, int* lo, int* hi) {
-  *hi = (min(q0 + 127, L - 1) >> 7) + 1;
-  *lo = window > 0 ? max(0, q0 - window + 1) >> 7 : 0;
+// Key tiles [lo, hi) visited by the 128-query tile at q0 of a sequence of L new tokens that
+// continue P cached keys (positions P .. P + L - 1).
+__device__ __forceinline__ void tile_keys(int q0, int L, int P, int window, int* lo, int* hi) {
+  *hi = ((P + min(q0 + 127, L - 1)) >> 7) + 1;
+  *lo = window > 0 ? max(0, P + q0 - window + 1) >> 7 : 0;
 }
 
 // One block lists the work items of every sequence, heaviest first (a counting sort on the
@@ -673,7 +704,7 @@ struct TileLists {
 
 __global__ void __launch_bounds__(1024)
     k_attn_tiles(const int32_t* __restrict__ cu, int n_seqs, int max_work, int groups, int sms,
-                 TileLists lists, int32_t* zero, int n_zero) {
+                 TileLists lists, int32_t* zero, int n_zero, const int32_t* __restrict__ prefix) {
   pdl_trigger();
   pdl_wait();
   // block b builds list b; block 0 also clears the launches' counters
@@ -714,7 +745,7 @@ __global__ void __launch_bounds__(1024)
   for (int g = threadIdx.x; g < total; g += blockDim.x) {
     int s, q0, lo, hi;
     locate(g, &s, &q0);
-    tile_keys(q0, cu[s + 1] - cu[s], window, &lo, &hi);
+    tile_keys(q0, cu[s + 1] - cu[s], prefix ? prefix[s] : 0, window, &lo, &hi);
     mine += hi - lo;
   }
   atomicAdd(&wsum, mine);
@@ -728,7 +759,7 @@ __global__ void __launch_bounds__(1024)
   for (int g = threadIdx.x; g < total; g += blockDim.x) {
     int s, q0, lo, hi;
     locate(g, &s, &q0);
-    tile_keys(q0, cu[s + 1] - cu[s], window, &lo, &hi);
+    tile_keys(q0, cu[s + 1] - cu[s], prefix ? prefix[s] : 0, window, &lo, &hi);
     const int w = hi - lo;
     const int nc = w > C + kMergeTiles ? min((w + C - 1) / C, kMaxChunks) : 1;
     for (int c = 0; c < nc; ++c)
@@ -749,7 +780,8 @@ __global__ void __launch_bounds__(1024)
     int s, q0, lo, hi;
     locate(g, &s, &q0);
     const int L = cu[s + 1] - cu[s];
-    tile_keys(q0, L, window, &lo, &hi);
+    const int P = prefix ? prefix[s] : 0;
+    tile_keys(q0, L, P, window, &lo, &hi);
     const int w = hi - lo;
     const int nc = w > C + kMergeTiles ? min((w + C - 1) / C, kMaxChunks) : 1;
     int split = -1, slot0 = -1;
@@ -770,7 +802,9 @@ __global__ void __launch_bounds__(1024)
       t.n_chunks = nc;
       t.slot0 = slot0;
       t.split = split;
-      t.pad[0] = t.pad[1] = t.pad[2] = 0;
+      t.prefix = P;
+      t.seq = s;
+      t.pad = 0;
       tiles[slot] = t;
     }
   }
@@ -794,8 +828,9 @@ int attn_max_tiles(int tokens, int n_seqs) { return (tokens + 127) / 128 + n_seq
 cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int groups,
                             int window_a, AttnTile* tiles_a, int32_t* n_tiles_a, int window_b,
                             AttnTile* tiles_b, int32_t* n_tiles_b, int32_t* zero, int n_zero,
-                            cudaStream_t s) {
-  const int max_work = (tokens + 127) / 128 + 1;
+                            cudaStream_t s, const int32_t* prefix, int max_prefix) {
+  // key tiles of a query tile: at most (longest prefix + tokens) / 128 + 2
+  const int max_work = (max_prefix + tokens + 127) / 128 + 1;
   const size_t smem = (size_t)(n_seqs + 1 + max_work + 1) * sizeof(int);
   if (groups <= 0 || !tiles_a || !n_tiles_a || n_zero < 0) return CC_ERR_INVALID_ARG;
   if (smem > 200 * 1024) return CC_ERR_UNSUPPORTED;
@@ -811,14 +846,15 @@ cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, i
   lists.n_tiles[1] = n_tiles_b;
   const int blocks = tiles_b ? 2 : 1;
   CC_CHECK_CUDA(launch_pdl(k_attn_tiles, dim3(blocks), dim3(1024), smem, s, cu_seqlens, n_seqs,
-                          max_work, groups, num_sms(), lists, zero, n_zero));
+                          max_work, groups, num_sms(), lists, zero, n_zero, prefix));
   return CC_OK;
 }
 
 cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               __nv_bfloat16* out, int ld_out, const AttnTile* tiles,
                               const int32_t* n_tiles, int max_tiles, int n_q, int n_kv,
-                              int window, const AttnScratch& sc, int* err, cudaStream_t s) {
+                              int window, const AttnScratch& sc, int* err, cudaStream_t s,
+                              const AttnPaged& paged) {
   static bool attr_set = false;
   if (!attr_set) {
     CC_CHECK_CUDA(cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -832,7 +868,7 @@ cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
   const long long items = (long long)max_tiles * attn_groups(n_q, n_kv);
   const int grid = static_cast<int>(std::min<long long>(items, num_sms()));
   CC_CHECK_CUDA(launch_pdl(k_attn_prefill, dim3(grid), dim3(kThreads), kSmem, s, tq, tk, tv, out,
-                          ld_out, tiles, n_tiles, n_q, n_kv, window, scale_log2, sc, err));
+                          ld_out, tiles, n_tiles, n_q, n_kv, window, scale_log2, sc, paged, err));
   return CC_OK;
 }
 

@@ -66,7 +66,17 @@ struct AttnTile {
   int32_t n_chunks;
   int32_t slot0;      // partial slot of chunk 0 (chunk c uses slot0 + c); -1 when unsplit
   int32_t split;      // ordinal of the split query tile (its arrival counters); -1 unsplit
-  int32_t pad[3];
+  int32_t prefix;     // keys of the sequence before this call's tokens (chunked prefill)
+  int32_t seq;        // the sequence (its page-table row)
+  int32_t pad;
+};
+
+// K and V of a chunked prefill: the paged pool [page][kv head][16][128] read through the
+// page table (pt null: contiguous K and V of the call's own tokens).
+struct AttnPaged {
+  const int32_t* pt = nullptr;  // [n_seqs, max_pages]
+  int max_pages = 0;
+  int n_pages = 0;
 };
 
 // Scratch of one prefill attention launch. `counters` and `sched` must be zero when the
@@ -94,18 +104,23 @@ int attn_counter_ints(int groups);
 // Builds the work lists of all sequences (query tiles, long ones cut into chunks), heaviest
 // first, for launches with `groups` head groups: list a with window_a and, when tiles_b is
 // not null, list b with window_b, in one launch that also zeroes zero[0 .. n_zero).
+// prefix (nullable, [n_seqs]): the tokens of sequence s continue a cached prefix of
+// prefix[s] keys (chunked prefill); the key tiles are then absolute key positions.
 cc_status launch_attn_tiles(const int32_t* cu_seqlens, int n_seqs, int tokens, int groups,
                             int window_a, AttnTile* tiles_a, int32_t* n_tiles_a, int window_b,
                             AttnTile* tiles_b, int32_t* n_tiles_b, int32_t* zero, int n_zero,
-                            cudaStream_t s);
+                            cudaStream_t s, const int32_t* prefix = nullptr, int max_prefix = 0);
 int attn_max_tiles(int tokens, int n_seqs);
 // Rows (keys) of the K and V boxes the prefill attention kernel loads.
 int attn_kv_box_rows();
 
+// tk, tv: [T, n_kv * 128] (contiguous) or, with paged.pt, the pools as
+// [n_pages * n_kv * 16, 128] with 16-row boxes.
 cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               __nv_bfloat16* out, int ld_out, const AttnTile* tiles,
                               const int32_t* n_tiles, int max_tiles, int n_q, int n_kv,
-                              int window, const AttnScratch& sc, int* err, cudaStream_t s);
+                              int window, const AttnScratch& sc, int* err, cudaStream_t s,
+                              const AttnPaged& paged = AttnPaged());
 
 // ---------------------------------------------------------------- decode attention
 struct DecodeScratch {
@@ -137,9 +152,12 @@ cc_status launch_embed_ln(const int32_t* tok, const __nv_bfloat16* embed, int V,
 cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, int* err,
                         cudaStream_t s);
 // kv_slot for prefill tokens: page_table[seq, t / ps] * ps + t % ps
+// slots[t] = cache slot of token t: position prefix[s] + (t - cu[s]) of its sequence s
+// (prefix nullable: 0).
 cc_status launch_kv_slots_prefill(const int32_t* cu_seqlens, int n_seqs, int T,
                                   const int32_t* page_table, int max_pages, int page_size,
-                                  int n_pages, int32_t* slots, int* err, cudaStream_t s);
+                                  int n_pages, int32_t* slots, int* err, cudaStream_t s,
+                                  const int32_t* prefix = nullptr);
 // kv_slot of decode rows: the new token of sequence b goes to slot seq_lens[b]
 cc_status launch_kv_slots_decode(const int32_t* seq_lens, int batch, const int32_t* page_table,
                                  int max_pages, int page_size, int n_pages, int32_t* slots,

@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(1024)
 
 __global__ void k_kv_slots_prefill(const int32_t* __restrict__ cu, int n_seqs, int T,
                                    const int32_t* __restrict__ pt, int max_pages, int ps,
-                                   int n_pages, int32_t* __restrict__ slots, int* err) {
+                                   int n_pages, int32_t* __restrict__ slots, int* err,
+                                   const int32_t* __restrict__ prefix) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -224,10 +225,10 @@ __global__ void k_kv_slots_prefill(const int32_t* __restrict__ cu, int n_seqs, i
     const int mid = (lo + hi) >> 1;
     if (cu[mid] <= t) lo = mid; else hi = mid;
   }
-  const int pos = t - cu[lo];
+  const int pos = t - cu[lo] + (prefix ? prefix[lo] : 0);
   const int pi = pos / ps;
   int slot = -1;
-  if (pi < max_pages) {
+  if (pos >= 0 && pi < max_pages) {
     const int page = pt[(size_t)lo * max_pages + pi];
     if (page >= 0 && page < n_pages) slot = page * ps + (pos - pi * ps);
   }
@@ -321,10 +322,12 @@ cc_status launch_ds_map(const int32_t* rows, int n_rows, int T, int32_t* map, in
 
 cc_status launch_kv_slots_prefill(const int32_t* cu_seqlens, int n_seqs, int T,
                                   const int32_t* page_table, int max_pages, int page_size,
-                                  int n_pages, int32_t* slots, int* err, cudaStream_t s) {
+                                  int n_pages, int32_t* slots, int* err, cudaStream_t s,
+                                  const int32_t* prefix) {
   if (T <= 0) return CC_OK;
   CC_CHECK_CUDA(launch_pdl(k_kv_slots_prefill, dim3((T + 255) / 256), dim3(256), 0, s, cu_seqlens,
-                            n_seqs, T, page_table, max_pages, page_size, n_pages, slots, err));
+                            n_seqs, T, page_table, max_pages, page_size, n_pages, slots, err,
+                            prefix));
   return CC_OK;
 }
 

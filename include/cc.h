@@ -189,6 +189,24 @@ cc_status cc_prefill_forward_tokens(cc_layer_plan* plan, const int32_t* token_id
                                     int32_t n_deepstack, const cc_kv_pool* kv,
                                     const int32_t* page_table, int32_t max_pages, void* stream);
 
+/* Chunked prefill (the step after a prefill chunk, before decode): as cc_prefill_forward,
+ * but the tokens of sequence s continue prefix_lens[s] keys already in the paged cache,
+ * at positions prefix_lens[s] .. prefix_lens[s] + L_s - 1 (pos_thw holds their absolute
+ * position ids, e.g. the slice of the whole sequence's ids, so an image span may cross the
+ * chunk boundary). Their keys and values are written to the cache at those slots and every
+ * query attends over the cached keys it sees (causal, window on sliding layers) through the
+ * page table; the result equals the rows of a prefill of the whole sequences.
+ *  prefix_lens int32 [n_seqs] (device); kv and page_table required,
+ *  prefix_lens[s] + L_s <= max_pages * 16. bf16 plans with head_dim 128 and 16-token pages
+ *  only (CC_ERR_UNSUPPORTED otherwise). */
+cc_status cc_prefill_forward_chunk(cc_layer_plan* plan, float* hidden, const int32_t* pos_thw,
+                                   const int32_t* cu_seqlens, int32_t n_seqs,
+                                   int32_t total_tokens, const int32_t* prefix_lens,
+                                   const int32_t* ds_rows, int32_t n_ds_rows,
+                                   const void* const* ds_feats, int32_t n_deepstack,
+                                   const cc_kv_pool* kv, const int32_t* page_table,
+                                   int32_t max_pages, void* stream);
+
 /* One decode step: one new token per sequence.
  *  hidden    f32 [batch, H] (in: the new tokens' embeddings; out: final h)
  *  pos_thw   int32 [3, batch] (cc_build_decode_positions)

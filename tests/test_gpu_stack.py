@@ -188,6 +188,60 @@ def test_decode_continues_prefill_on_gpu():
     assert mx <= TOL_MAX and mn <= TOL_MEAN, (mx, mn)
 
 
+def test_chunked_prefill_over_a_paged_prefix():
+    """Two sequences prefilled in two chunks each (an image span crosses each boundary,
+    deepstack rows on both sides): the first chunk fills the paged cache, the second
+    continues it through cc_prefill_forward_chunk. Both chunks' rows equal the rows of the
+    whole prefill (on the GPU and in the oracle)."""
+    types = (SLIDING, FULL, SLIDING)
+    lens, cut = [300, 200], [130, 77]
+    imgs = [ImageSpan(0, 120, 1, 4, 6), ImageSpan(1, 60, 1, 5, 5), ImageSpan(1, 150, 1, 2, 3)]
+    full = _small("chunked", lens, imgs, 1, types=types, window=90, head_rows="all", seed=43)
+    gw, h_full, _ = _run(full)
+    h_ref, _ = R.run_prefill(full)
+    st = gw.stack
+    s = full.shape
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    rows1 = np.concatenate([np.arange(starts[i], starts[i] + cut[i]) for i in range(2)])
+    rows2 = np.concatenate([np.arange(starts[i] + cut[i], starts[i + 1]) for i in range(2)])
+    pos_full = gw.pos.cpu().numpy()
+    ds_rows_full = full.ds_rows
+    ps, max_pages = 16, (max(lens) + 15) // 16
+    n_pages = 2 * max_pages + 3
+    table = torch.tensor(np.random.default_rng(2).permutation(n_pages)[:2 * max_pages]
+                         .reshape(2, max_pages), dtype=torch.int32, device="cuda")
+    kp = [torch.zeros(n_pages, s.num_key_value_heads, ps, 128, dtype=torch.bfloat16,
+                      device="cuda") for _ in types]
+    vp = [torch.zeros_like(t) for t in kp]
+    kv = L.make_kv_pool(kp, vp, n_pages)
+
+    def chunk_inputs(rows, seq_lens):
+        h = torch.from_numpy(full.hidden[rows].copy()).cuda()
+        pos = torch.from_numpy(np.ascontiguousarray(pos_full[:, rows])).cuda()
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(seq_lens)]), dtype=torch.int32,
+                          device="cuda")
+        where = {int(r): k for k, r in enumerate(rows)}
+        sel = [k for k, r in enumerate(ds_rows_full) if int(r) in where]
+        ds_rows = torch.tensor([where[int(ds_rows_full[k])] for k in sel], dtype=torch.int32,
+                               device="cuda")
+        ds = [to_device(full.ds(0)[sel])]
+        return h, pos, cu, ds_rows, ds
+
+    h1, pos1, cu1, dr1, ds1 = chunk_inputs(rows1, cut)
+    L.cc_prefill_forward(st.plan, h1, pos1, cu1, 2, len(rows1), dr1, int(dr1.numel()), ds1, kv,
+                         table, max_pages)
+    len2 = [lens[i] - cut[i] for i in range(2)]
+    h2, pos2, cu2, dr2, ds2 = chunk_inputs(rows2, len2)
+    prefix = torch.tensor(cut, dtype=torch.int32, device="cuda")
+    L.cc_prefill_forward_chunk(st.plan, h2, pos2, cu2, 2, len(rows2), prefix, kv, table,
+                               max_pages, dr2, int(dr2.numel()), ds2)
+    st.sync()
+    hf = as_numpy(h_full)
+    for got, rows in ((h1, rows1), (h2, rows2)):
+        assert_close(as_numpy(got), hf[rows], TOL_MAX, TOL_MEAN, "chunk vs whole prefill")
+        assert_close(as_numpy(got), h_ref[rows], TOL_MAX, TOL_MEAN, "chunk vs oracle")
+
+
 @pytest.fixture(scope="module")
 def cfg3_oracle():
     """The 28-layer workload's inputs and the oracle's residual stream after every layer."""
