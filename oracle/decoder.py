@@ -198,6 +198,32 @@ def embed_merge(token_ids, embed, mm_rows=None, mm_embeds=None):
 
 
 # ----------------------------------------------------------------------------------
+# 4-bit affine weights ([Compass issue] "Config (config.json)": quantization {group_size 64,
+# bits 4, mode affine} in the mlx conversion that the reference checkpoint ships)
+# ----------------------------------------------------------------------------------
+def dequantize_affine(packed, scales, biases, group=64, bits=4):
+    """w[n, k] = scales[n, k // group] * q[n, k] + biases[n, k // group].
+
+    Readings: q[n, k] is the bits-wide field at bit offset bits * (k % (32 // bits)) of the
+    32-bit word packed[n, k // (32 // bits)] (lowest bits first); scales and biases are the
+    stored values (bf16 bit patterns or floats). The result is exact (float64).
+    """
+    packed = np.asarray(packed, dtype=np.uint32)
+    per = 32 // bits
+    N, W = packed.shape
+    K = W * per
+    q = np.empty((N, K), dtype=np.float64)
+    mask = np.uint32((1 << bits) - 1)
+    for i in range(per):
+        q[:, i::per] = ((packed >> np.uint32(bits * i)) & mask).astype(np.float64)
+    s = from_storage(scales)
+    b = from_storage(biases)
+    if s.shape != (N, K // group) or b.shape != (N, K // group):
+        raise ValueError("scales / biases must hold one value per group of each row")
+    return np.repeat(s, group, axis=1) * q + np.repeat(b, group, axis=1)
+
+
+# ----------------------------------------------------------------------------------
 # a2: LayerNorm ([Compass issue], "Text decoder forward": weight only, no bias)
 # ----------------------------------------------------------------------------------
 def layer_norm(x, gamma, eps):

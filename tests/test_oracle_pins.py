@@ -438,3 +438,17 @@ def test_embed_merge_without_images_is_the_lookup_and_rejects_bad_input():
         O.embed_merge([1, 2, 3], embed, [1, 1], np.zeros((2, 8)))
     with pytest.raises(ValueError):
         O.embed_merge([1, 2, 3], embed, [3], np.zeros((1, 8)))
+
+
+# ---------------------------------------------------------------- 4-bit affine weights
+def test_dequantize_affine_worked_example():
+    g = read_golden("affine_q4_row.txt")
+    packed = np.array([g["words"]], dtype=np.uint64).astype(np.uint32)
+    w = O.dequantize_affine(packed, np.array([g["scales"]]), np.array([g["biases"]]))
+    assert w.shape == (1, 128)
+    assert w[0, :16].tolist() == g["w_first16"]
+    assert w[0, 32:36].tolist() == g["w_32_35"]
+    assert np.all(w[0, 64:] == g["w_group1"][0])
+    # the descending half of group 0: q = 15 - (k - 16)
+    assert w[0, 16:32].tolist() == [0.5 * (15 - i) - 2.0 for i in range(16)]
+    assert np.all(w[0, 48:64] == 0.5 * 7 - 2.0)
