@@ -56,6 +56,7 @@ def parse():
     p.add_argument("--no-prefill", action="store_true", help="decode leg only (profiling)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-q4", action="store_true", help="skip the 4-bit weight decode timing")
     p.add_argument("--cpu-tokens", type=int, default=0,
                    help="oracle sample: first N tokens of the prefill workload (0: all)")
     p.add_argument("--prefill-config", type=int, choices=[2, 3, 5], default=2,
@@ -479,8 +480,68 @@ def decode_leg(args, dist, pk):
     value = B * K * dist.world / (ms / 1e3)
     launches = sum(v["launches_per_step"] for v in kern.values())
     launches += kern.get("attn_decode", {}).get("launches_per_step", 0)  # + split combine
+    res = dict(ms=ms, value=value, kernels=kern, roofline=roof, launches=int(round(launches * K)))
+    if not args.no_q4:
+        res["next_rows"] = {"decode_q4": decode_q4_timing(inp, gw, pk)}
     gw.close()
-    return dict(ms=ms, value=value, kernels=kern, roofline=roof, launches=int(round(launches * K)))
+    return res
+
+
+def decode_q4_timing(inp, gw, pk, steps=10):
+    """The decode step + head on 4-bit affine weights (group 64): the same workload and
+    cache, weights streamed at a quarter of their bf16 bytes; per GEMM class the weight
+    stream's bandwidth against the HBM roof."""
+    import torch
+    import cohere_compass_decoder_gb300._lib as L
+    s = inp.shape
+    st = gw.stack
+    st.attach_q4(inp.layer_q4, inp.embed_q4)
+    B = inp.wl.decode_batch
+    n = int(gw.head_rows.numel())
+    lg = torch.empty(n, s.vocab_size, dtype=torch.float32, device="cuda")
+    pool = [gw.fresh_hidden() for _ in range(steps + 3)]
+
+    def run(i):
+        st.decode_q4(pool[i], gw.pos, gw.seq_lens, gw.page_table, gw.max_pages, gw.kv)
+        st.logits_q4(pool[i], gw.head_rows, n, lg)
+    for i in range(3):
+        run(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        run(3 + i)
+    e1.record()
+    torch.cuda.synchronize()
+    st.sync()
+    ms = e0.elapsed_time(e1) / steps
+    for i in range(steps):
+        pool[3 + i].copy_(gw.hidden0)
+    L.cc_profile_read(st.plan)
+    L.cc_profile_enable(st.plan, True)
+    for i in range(steps):
+        run(3 + i)
+    torch.cuda.synchronize()
+    prof = L.cc_profile_read(st.plan)
+    L.cc_profile_enable(st.plan, False)
+    H, V = s.hidden_size, s.vocab_size
+    N1 = (s.num_attention_heads + 2 * s.num_key_value_heads) * s.head_dim + 2 * s.intermediate_size
+    K2 = s.num_attention_heads * s.head_dim + s.intermediate_size
+
+    def wbytes(N, K):       # packed words + (scale, bias) words
+        return N * K // 2 + N * (K // 64) * 4
+    per = {"gemm_qkv_mlp": wbytes(N1, H), "gemm_out_resid": wbytes(H, K2),
+           "gemm_head": wbytes(V, H)}
+    out = {}
+    for name, nb in per.items():
+        cnt, tot = prof.get(name, (0, 0.0))
+        if cnt:
+            us = 1000.0 * tot / cnt
+            out[name] = {"avg_us": us, "weight_bytes": nb, "gbs": nb / (us * 1e-6) / 1e9,
+                         "frac_of_hbm": nb / (us * 1e-6) / 1e9 / pk["hbm"]}
+    return {"ms_per_step": ms, "tokens_per_s": B / (ms / 1e3), "kernels": out,
+            "note": "cc_decode_step_q4 + cc_logits_q4 on the decode workload (64 sequences, "
+                    "4096 cached tokens each); gbs counts the 4-bit weight stream only"}
 
 
 def cpu_baseline(args, tokens=0):
@@ -582,6 +643,8 @@ def main():
             line["decode"] = {"workload": DECODE_DESC, "value": dec["value"], "unit": "tokens/s",
                               "ms_per_step": dec["ms"] / args.steps, "roofline": dec["roofline"],
                               "gpu_launches": dec["launches"], "kernels": dec["kernels"]}
+            if dec.get("next_rows"):
+                line.setdefault("next_rows", {}).update(dec["next_rows"])
         print(json.dumps(line))
     dist.close()
     return 0

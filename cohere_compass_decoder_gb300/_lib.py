@@ -24,7 +24,9 @@ EXPORTS = [
     "cc_op_mrope_table", "cc_op_gemm_bf16", "cc_op_attention_prefill",
     "cc_op_attention_decode", "cc_op_sync", "cc_profile_enable", "cc_profile_read",
     "cc_kernel_class_name", "cc_op_attention_decode_noalloc", "cc_prefill_forward_tokens",
-    "cc_op_embed_merge", "cc_prefill_forward_chunk",
+    "cc_op_embed_merge", "cc_prefill_forward_chunk", "cc_q4_tiled_bytes", "cc_pack_q4_tiles",
+    "cc_pack_layer_weights_q4", "cc_layer_plan_attach_q4", "cc_decode_step_q4", "cc_logits_q4",
+    "cc_op_gemm_q4",
 ]
 KERNEL_CLASSES = ["rope_table", "row_maps", "layernorm", "gemm_qkv_mlp", "attn_prefill",
                   "gemm_out_resid", "attn_decode", "gemm_head", "f32_path", "embed_merge"]
@@ -48,6 +50,10 @@ class cc_model_config(C.Structure):
 
 
 class cc_layer_weights(C.Structure):
+    _fields_ = [("ln_w", C.c_void_p), ("w1", C.c_void_p), ("w2", C.c_void_p)]
+
+
+class cc_layer_weights_q4(C.Structure):
     _fields_ = [("ln_w", C.c_void_p), ("w1", C.c_void_p), ("w2", C.c_void_p)]
 
 
@@ -98,6 +104,15 @@ def lib() -> C.CDLL:
             "cc_decode_step": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, C.POINTER(cc_kv_pool), vp]),
             "cc_logits": (C.c_int, [vp, vp, vp, i32, vp, vp]),
             "cc_sync": (C.c_int, [vp, vp]),
+            "cc_q4_tiled_bytes": (C.c_size_t, [i32, i32]),
+            "cc_pack_q4_tiles": (C.c_int, [vp, vp, vp, i32, i32, vp, vp]),
+            "cc_pack_layer_weights_q4": (C.c_int, [C.POINTER(cc_model_config), C.POINTER(vp),
+                                                   C.POINTER(vp), C.POINTER(vp), vp, vp, vp]),
+            "cc_layer_plan_attach_q4": (C.c_int, [vp, C.POINTER(cc_layer_weights_q4), vp]),
+            "cc_decode_step_q4": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, C.POINTER(cc_kv_pool),
+                                            vp]),
+            "cc_logits_q4": (C.c_int, [vp, vp, vp, i32, vp, vp]),
+            "cc_op_gemm_q4": (C.c_int, [vp, vp, vp, i32, i32, i32, C.c_float, i32, vp]),
             "cc_op_layernorm": (C.c_int, [vp, vp, vp, i32, i32, C.c_float, vp, vp]),
             "cc_op_embed_merge": (C.c_int, [vp, i32, vp, i32, i32, vp, vp, i32, vp, vp, C.c_float,
                                             vp, vp]),
@@ -287,6 +302,43 @@ def cc_logits(plan, hidden, rows, n_rows, logits, stream=None):
     _check(st, "cc_logits")
 
 
+def cc_q4_tiled_bytes(rows, k):
+    return int(lib().cc_q4_tiled_bytes(rows, k))
+
+
+def cc_pack_q4_tiles(words, scales, biases, rows, k, out, stream=None):
+    _check(lib().cc_pack_q4_tiles(_ptr(words), _ptr(scales), _ptr(biases), rows, k, _ptr(out),
+                                  _stream(stream)), "cc_pack_q4_tiles")
+
+
+def cc_pack_layer_weights_q4(cfg, packed, scales, biases, w1_out, w2_out, stream=None):
+    """packed / scales / biases: 7 tensors each, in the order q, k, v, o, gate, up, down."""
+    arrs = [(C.c_void_p * 7)(*[_ptr(t) for t in group]) for group in (packed, scales, biases)]
+    st = lib().cc_pack_layer_weights_q4(C.byref(cfg), *arrs, _ptr(w1_out), _ptr(w2_out),
+                                        _stream(stream))
+    _check(st, "cc_pack_layer_weights_q4")
+
+
+def cc_layer_plan_attach_q4(plan, layers, embed_q4):
+    """layers: sequence of (ln_w, w1, w2) tensors (tiled 4-bit weights)."""
+    arr = (cc_layer_weights_q4 * len(layers))()
+    for i, t in enumerate(layers):
+        arr[i] = cc_layer_weights_q4(*[_ptr(x) for x in t])
+    _check(lib().cc_layer_plan_attach_q4(plan, arr, _ptr(embed_q4)), "cc_layer_plan_attach_q4")
+
+
+def cc_decode_step_q4(plan, hidden, pos_thw, seq_lens, page_table, max_pages, batch, kv,
+                      stream=None):
+    st = lib().cc_decode_step_q4(plan, _ptr(hidden), _ptr(pos_thw), _ptr(seq_lens),
+                                 _ptr(page_table), max_pages, batch, C.byref(kv), _stream(stream))
+    _check(st, "cc_decode_step_q4")
+
+
+def cc_logits_q4(plan, hidden, rows, n_rows, logits, stream=None):
+    st = lib().cc_logits_q4(plan, _ptr(hidden), _ptr(rows), n_rows, _ptr(logits), _stream(stream))
+    _check(st, "cc_logits_q4")
+
+
 def cc_sync(plan, stream=None):
     _check(lib().cc_sync(plan, _stream(stream)), "cc_sync")
 
@@ -309,6 +361,11 @@ def cc_op_mrope_table(pos, tokens, head_dim, theta, section, table, stream=None)
 def cc_op_gemm_bf16(a, b, c, m, n, k, alpha=1.0, accumulate=0, stream=None):
     _check(lib().cc_op_gemm_bf16(_ptr(a), _ptr(b), _ptr(c), m, n, k, alpha, accumulate,
                                  _stream(stream)), "cc_op_gemm_bf16")
+
+
+def cc_op_gemm_q4(a, w_tiled, c, m, n, k, alpha=1.0, accumulate=0, stream=None):
+    _check(lib().cc_op_gemm_q4(_ptr(a), _ptr(w_tiled), _ptr(c), m, n, k, alpha, accumulate,
+                               _stream(stream)), "cc_op_gemm_q4")
 
 
 def cc_op_embed_merge(token_ids, tokens, embed, vocab, hidden_size, mm_rows, mm_embeds,

@@ -184,6 +184,9 @@ struct cc_layer_plan {
   int32_t* attn_cnt = nullptr;
   size_t attn_cnt_ints = 0;
   int attn_groups_n = 1;
+  // tiled 4-bit affine weights (cc_layer_plan_attach_q4)
+  std::vector<cc_layer_weights_q4> layers_q4;
+  const void* embed_q4 = nullptr;
   // decode split-KV scratch, grown on demand
   float* dec_scratch = nullptr;
   size_t dec_scratch_floats = 0;
@@ -376,6 +379,106 @@ extern "C" cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_l
 }
 
 extern "C" void cc_layer_plan_destroy(cc_layer_plan* plan) { delete plan; }
+
+extern "C" size_t cc_q4_tiled_bytes(int32_t rows, int32_t k) {
+  if (rows <= 0 || k <= 0 || rows % 128 != 0 || k % 64 != 0) return 0;
+  return q4_tiled_bytes(rows, k);
+}
+
+extern "C" cc_status cc_pack_q4_tiles(const void* words, const void* scales, const void* biases,
+                                      int32_t rows, int32_t k, void* out, void* stream) {
+  if (rows < 0 || k < 0) return CC_ERR_INVALID_ARG;
+  if (rows == 0 || k == 0) return CC_OK;
+  if (rows % 128 != 0 || k % 64 != 0) return CC_ERR_UNSUPPORTED;
+  if (!words || !scales || !biases || !out) return CC_ERR_INVALID_ARG;
+  return launch_q4_tile(static_cast<const uint32_t*>(words), static_cast<const uint16_t*>(scales),
+                        static_cast<const uint16_t*>(biases), rows, k, static_cast<uint8_t*>(out),
+                        static_cast<cudaStream_t>(stream));
+}
+
+extern "C" cc_status cc_pack_layer_weights_q4(const cc_model_config* cfg, const void* const* packed,
+                                              const void* const* scales, const void* const* biases,
+                                              void* w1_out, void* w2_out, void* stream) {
+  CC_CHECK_STATUS(check_config(cfg));
+  if (cfg->dtype != CC_BF16) return CC_ERR_UNSUPPORTED;
+  if (!packed || !scales || !biases || !w1_out || !w2_out) return CC_ERR_INVALID_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (!packed[i] || !scales[i] || !biases[i]) return CC_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t H = cfg->hidden_size, d = cfg->head_dim, I = cfg->intermediate_size;
+  const size_t qr = cfg->n_q_heads * d, kr = cfg->n_kv_heads * d, K2 = qr + I;
+  const size_t N1 = qr + 2 * kr + 2 * I;
+  // the fused matrices in checkpoint (row-major) form first: w1 [N1, H] rows q | k | v | gate
+  // and up in 64-row blocks, w2 [H, K2] columns o | down; then their tiles
+  const size_t w1_words = N1 * H / 8, w1_groups = N1 * H / 64;
+  const size_t w2_words = H * K2 / 8, w2_groups = H * K2 / 64;
+  uint8_t* tmp = nullptr;
+  const size_t tmp_bytes = std::max(w1_words * 4 + 2 * w1_groups * 2, w2_words * 4 + 2 * w2_groups * 2);
+  CC_CHECK_CUDA(cudaMallocAsync(&tmp, tmp_bytes, s));
+  cc_status st = CC_OK;
+  auto fail = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == CC_OK) {
+      last_cuda_error() = e;
+      st = CC_ERR_CUDA;
+    }
+  };
+  const cudaMemcpyKind dd = cudaMemcpyDeviceToDevice;
+  {
+    // three parts with the row arrangement of w1: words (H / 2 bytes per row), scales and
+    // biases (H / 32 bytes per row)
+    uint8_t* parts[3] = {tmp, tmp + w1_words * 4, tmp + w1_words * 4 + w1_groups * 2};
+    const size_t row_b[3] = {H / 2, H / 32, H / 32};
+    const void* const* src[3] = {packed, scales, biases};
+    for (int q = 0; q < 3; ++q) {
+      uint8_t* base = parts[q];
+      const size_t row = row_b[q];
+      fail(cudaMemcpyAsync(base, src[q][0], qr * row, dd, s));
+      fail(cudaMemcpyAsync(base + qr * row, src[q][1], kr * row, dd, s));
+      fail(cudaMemcpyAsync(base + (qr + kr) * row, src[q][2], kr * row, dd, s));
+      uint8_t* mlp = base + (qr + 2 * kr) * row;
+      fail(cudaMemcpy2DAsync(mlp, 128 * row, src[q][4], 64 * row, 64 * row, I / 64, dd, s));
+      fail(cudaMemcpy2DAsync(mlp + 64 * row, 128 * row, src[q][5], 64 * row, 64 * row, I / 64, dd, s));
+    }
+    if (st == CC_OK)
+      st = launch_q4_tile(reinterpret_cast<const uint32_t*>(parts[0]),
+                          reinterpret_cast<const uint16_t*>(parts[1]),
+                          reinterpret_cast<const uint16_t*>(parts[2]), static_cast<int>(N1),
+                          static_cast<int>(H), static_cast<uint8_t*>(w1_out), s);
+  }
+  if (st == CC_OK) {
+    // w2's columns: o then down, per part (words: 1/2 byte per column; scales, biases: 1/32)
+    uint8_t* parts[3] = {tmp, tmp + w2_words * 4, tmp + w2_words * 4 + w2_groups * 2};
+    const void* const* src[3] = {packed, scales, biases};
+    for (int q = 0; q < 3; ++q) {
+      const size_t per = q == 0 ? 2 : 32;   // columns per byte of the part
+      fail(cudaMemcpy2DAsync(parts[q], K2 / per, src[q][3], qr / per, qr / per, H, dd, s));
+      fail(cudaMemcpy2DAsync(parts[q] + qr / per, K2 / per, src[q][6], I / per, I / per, H, dd, s));
+    }
+    if (st == CC_OK)
+      st = launch_q4_tile(reinterpret_cast<const uint32_t*>(parts[0]),
+                          reinterpret_cast<const uint16_t*>(parts[1]),
+                          reinterpret_cast<const uint16_t*>(parts[2]), static_cast<int>(H),
+                          static_cast<int>(K2), static_cast<uint8_t*>(w2_out), s);
+  }
+  fail(cudaFreeAsync(tmp, s));
+  return st;
+}
+
+extern "C" cc_status cc_layer_plan_attach_q4(cc_layer_plan* p, const cc_layer_weights_q4* layers,
+                                             const void* embed_q4) {
+  if (!p || !layers || !embed_q4) return CC_ERR_INVALID_ARG;
+  if (!p->bf16) return CC_ERR_UNSUPPORTED;
+  auto aligned = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  const int L = p->cfg.num_layers;
+  for (int i = 0; i < L; ++i)
+    if (!layers[i].ln_w || !layers[i].w1 || !layers[i].w2 || !aligned(layers[i].w1) ||
+        !aligned(layers[i].w2))
+      return CC_ERR_INVALID_ARG;
+  if (!aligned(embed_q4)) return CC_ERR_INVALID_ARG;
+  p->layers_q4.assign(layers, layers + L);
+  p->embed_q4 = embed_q4;
+  return CC_OK;
+}
 
 // one GEMM with the plan's tile choice; `b128`/`b256` are the weight maps
 // Rows declared in the tensor map of a workspace activation (a, a2) for an m-row GEMM: at
@@ -617,13 +720,13 @@ extern "C" cc_status cc_prefill_forward_chunk(
                       nullptr, prefix_lens);
 }
 
-extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32_t* pos_thw,
-                                    const int32_t* seq_lens, const int32_t* page_table,
-                                    int32_t max_pages, int32_t batch, const cc_kv_pool* kv,
-                                    void* stream) {
+static cc_status decode_step(cc_layer_plan* p, float* hidden, const int32_t* pos_thw,
+                             const int32_t* seq_lens, const int32_t* page_table, int32_t max_pages,
+                             int32_t batch, const cc_kv_pool* kv, void* stream, bool q4) {
   if (!p) return CC_ERR_INVALID_ARG;
   if (!p->bf16) return CC_ERR_UNSUPPORTED;
   if (batch < 0 || batch > p->T_max) return CC_ERR_INVALID_ARG;
+  if (q4 && (p->layers_q4.empty() || batch > 128)) return CC_ERR_INVALID_ARG;
   if (batch == 0) return CC_OK;
   if (!hidden || !pos_thw || !seq_lens || !page_table || max_pages <= 0 || !kv || !kv->k ||
       !kv->v || kv->n_pages <= 0)
@@ -651,12 +754,14 @@ extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32
   CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_decode(seq_lens, batch, page_table, max_pages, c.kv_page_size,
                                          kv->n_pages, p->kv_slot, p->n_keys, p->err, s));
   CUtensorMap ta, ta2;
-  if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, batch), p->H, p->H, 128, 64) ||
-      !make_tmap_bf16_2d(&ta2, p->a2, act_rows(p, batch), p->K2, p->K2, 128, 64))
+  const uint32_t box = q4 ? static_cast<uint32_t>(gemm_q4_token_tile(batch)) : 128u;
+  if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, batch), p->H, p->H, box, 64) ||
+      !make_tmap_bf16_2d(&ta2, p->a2, act_rows(p, batch), p->K2, p->K2, box, 64))
     return CC_ERR_CUDA;
   for (int i = 0; i < c.num_layers; ++i) {
     const bool sliding = p->types[i] == CC_SLIDING;
-    CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(p->layers[i].ln_w),
+    const void* ln_w = q4 ? p->layers_q4[i].ln_w : p->layers[i].ln_w;
+    CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(ln_w),
                                           p->a, batch, p->H, c.layer_norm_eps, nullptr, s));
     EpiParams e1;
     e1.q_cols = p->q_cols;
@@ -671,8 +776,12 @@ extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32
     e1.page_size = c.kv_page_size;
     e1.act_out = p->a2 + p->q_cols;
     e1.ld_act = p->K2;
-    CC_TIMED(p, CC_K_GEMM_QKV_MLP, s, plan_gemm(ta, p->w1_128[i], p->w1_256[i], batch, p->N1, p->H, EPI_QKV_MLP, e1,
-                              p->err, s));
+    if (q4)
+      CC_TIMED(p, CC_K_GEMM_QKV_MLP, s, launch_gemm_q4(ta, p->layers_q4[i].w1, batch, p->N1, p->H,
+                                                      EPI_QKV_MLP, e1, p->err, s));
+    else
+      CC_TIMED(p, CC_K_GEMM_QKV_MLP, s, plan_gemm(ta, p->w1_128[i], p->w1_256[i], batch, p->N1, p->H, EPI_QKV_MLP, e1,
+                                p->err, s));
     CC_TIMED(p, CC_K_ATTN_DECODE, s, launch_attn_decode(p->q, p->q_cols, static_cast<const __nv_bfloat16*>(kv->k[i]),
                                        static_cast<const __nv_bfloat16*>(kv->v[i]), kv->n_pages,
                                        page_table, max_pages, p->n_keys, batch, p->nq, p->nkv,
@@ -681,10 +790,52 @@ extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32
     EpiParams e2;
     e2.c = hidden;
     e2.ldc = p->H;
-    CC_TIMED(p, CC_K_GEMM_OUT, s, plan_gemm(ta2, p->w2_128[i], p->w2_256[i], batch, p->H, p->K2, EPI_RESID, e2,
-                              p->err, s));
+    if (q4)
+      CC_TIMED(p, CC_K_GEMM_OUT, s, launch_gemm_q4(ta2, p->layers_q4[i].w2, batch, p->H, p->K2,
+                                                  EPI_RESID, e2, p->err, s));
+    else
+      CC_TIMED(p, CC_K_GEMM_OUT, s, plan_gemm(ta2, p->w2_128[i], p->w2_256[i], batch, p->H, p->K2, EPI_RESID, e2,
+                                p->err, s));
   }
   return CC_OK;
+}
+
+extern "C" cc_status cc_decode_step(cc_layer_plan* p, float* hidden, const int32_t* pos_thw,
+                                    const int32_t* seq_lens, const int32_t* page_table,
+                                    int32_t max_pages, int32_t batch, const cc_kv_pool* kv,
+                                    void* stream) {
+  return decode_step(p, hidden, pos_thw, seq_lens, page_table, max_pages, batch, kv, stream, false);
+}
+
+extern "C" cc_status cc_decode_step_q4(cc_layer_plan* p, float* hidden, const int32_t* pos_thw,
+                                       const int32_t* seq_lens, const int32_t* page_table,
+                                       int32_t max_pages, int32_t batch, const cc_kv_pool* kv,
+                                       void* stream) {
+  return decode_step(p, hidden, pos_thw, seq_lens, page_table, max_pages, batch, kv, stream, true);
+}
+
+extern "C" cc_status cc_logits_q4(cc_layer_plan* p, const float* hidden, const int32_t* rows,
+                                  int32_t n_rows, float* logits, void* stream) {
+  if (!p) return CC_ERR_INVALID_ARG;
+  if (!p->bf16) return CC_ERR_UNSUPPORTED;
+  if (p->layers_q4.empty() || n_rows < 0 || n_rows > p->T_max || n_rows > 128)
+    return CC_ERR_INVALID_ARG;
+  if (n_rows == 0) return CC_OK;
+  if (!hidden || !logits) return CC_ERR_INVALID_ARG;
+  const cc_model_config& c = p->cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(p->final_ln),
+                                        p->a, n_rows, p->H, c.layer_norm_eps, rows, s));
+  CUtensorMap ta;
+  if (!make_tmap_bf16_2d(&ta, p->a, act_rows(p, n_rows), p->H, p->H,
+                         static_cast<uint32_t>(gemm_q4_token_tile(n_rows)), 64))
+    return CC_ERR_CUDA;
+  EpiParams e;
+  e.c = logits;
+  e.ldc = p->V;
+  e.alpha = c.logit_scale;
+  ProfScope ps_(p->prof, CC_K_GEMM_HEAD, s);
+  return launch_gemm_q4(ta, p->embed_q4, n_rows, p->V, p->H, EPI_F32, e, p->err, s);
 }
 
 extern "C" cc_status cc_logits(cc_layer_plan* p, const float* hidden, const int32_t* rows,
@@ -791,6 +942,25 @@ extern "C" cc_status cc_op_gemm_bf16(const void* a, const void* b, float* c, int
   e.alpha = alpha;
   e.accumulate = accumulate || splits > 1;
   return launch_gemm(ta, tb, m, n, k, bn, splits, EPI_F32, e, op_error_flag(), s);
+}
+
+extern "C" cc_status cc_op_gemm_q4(const void* a, const void* w_tiled, float* c, int32_t m,
+                                   int32_t n, int32_t k, float alpha, int32_t accumulate,
+                                   void* stream) {
+  if (m < 0 || n <= 0 || k <= 0) return CC_ERR_INVALID_ARG;
+  if (m == 0) return CC_OK;
+  if (!a || !w_tiled || !c) return CC_ERR_INVALID_ARG;
+  if (m > 128 || k % 64 != 0 || n % 128 != 0) return CC_ERR_UNSUPPORTED;
+  CUtensorMap ta;
+  if (!make_tmap_bf16_2d(&ta, a, m, k, k, static_cast<uint32_t>(gemm_q4_token_tile(m)), 64))
+    return CC_ERR_INVALID_ARG;
+  EpiParams e;
+  e.c = c;
+  e.ldc = n;
+  e.alpha = alpha;
+  e.accumulate = accumulate != 0;
+  return launch_gemm_q4(ta, w_tiled, m, n, k, EPI_F32, e, op_error_flag(),
+                        static_cast<cudaStream_t>(stream));
 }
 
 extern "C" cc_status cc_op_attention_prefill(const void* q, const void* k, const void* v, void* out,

@@ -46,7 +46,6 @@ int num_sms();
 // Zero fill out of bounds. Returns false on failure (bad alignment or driver error).
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t ld, uint32_t box_rows, uint32_t box_cols);
-
 // Launches a kernel of the path with programmatic stream serialization: its CTAs may start
 // (barrier set-up, tensor-memory allocation) while the previous kernel on the stream
 // finishes; every kernel waits (griddepcontrol.wait) before it touches global memory and

@@ -370,6 +370,432 @@ cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
   return CC_OK;
 }
 
+// ------------------------------------------------------------------ 4-bit affine weights
+// C[M, N] (epilogue) = X[M, K] @ W[N, K]^T with W[n, k] = scale * q + bias per group of 64
+// along K (the mlx conversion's affine 4-bit weights, Compass issue "Config (config.json)"),
+// for decode-size M <= 128. Weight-stationary: each unit is 128 weight rows (the MMA's M side)
+// against all M tokens (its N side, BT = M rounded up to 16), so the tensor work scales with
+// the batch, and the weights stream from HBM at a quarter of their bf16 size. The weight
+// weights come pre-tiled (launch_q4_tile): the packed words and (scale, bias) words of 128
+// rows x 128 K are one contiguous 9 KB block, fetched with one bulk copy into a deep ring:
+//   warp 0       weight blocks, 12 stages
+//   warp 14      token tiles X (bf16, 128-byte swizzle) per 64-K block, 48 KB ring
+//   warp 1       MMA: 4 x tcgen05.mma (M=128, N=BT, K=16) per 64-K block, D = W X^T in TMEM
+//   warps 2..5   epilogue: TMEM lane = weight row, column = token
+//   warps 6..13  dequantisation: thread (r, h) turns row r of the h-th 64-K half of a packed
+//                stage into bf16 (a 3-stage ring of W tiles); each 32-bit word gives four
+//                bf16x2 pairs: the nibble pair goes into the mantissas of 128.0 (0x4300 | q
+//                is 128 + q in bf16), 128 is subtracted exactly and fma.rn.bf16x2(scale, q,
+//                bias) rounds scale * q + bias once.
+constexpr int kQ4Threads = 480;
+constexpr int kQ4Rows = 128;                          // weight rows per unit
+constexpr int kQ4QStages = 12;                        // packed words: 128 K per stage
+constexpr int kQ4WStages = 3;                         // dequantised bf16 tiles: 64 K per stage
+constexpr int kQ4XMaxStages = 8;                      // token tiles: 64 K per stage
+constexpr uint32_t kQ4QWords = kQ4Rows * 64;          // 8 KB: 128 rows x 64 bytes
+constexpr uint32_t kQ4QBytes = kQ4QWords + 2 * kQ4Rows * 4;   // + two groups' (scale, bias)
+static_assert(kQ4QBytes == kQ4TileBlockBytes, "tiled weight block");
+constexpr uint32_t kQ4WBytes = kQ4Rows * kBK * 2;     // 16 KB
+constexpr uint32_t kQ4XRing = 48 * 1024;              // token ring: 48 KB / (BT * 128) stages
+constexpr uint32_t kQ4ExBytes = 32 * kQ4Rows * 4;     // epilogue exchange: 32 tokens x 128 rows
+constexpr uint32_t kQ4OffX = kQ4WStages * kQ4WBytes;
+constexpr uint32_t kQ4OffQ = kQ4OffX + kQ4XRing;
+constexpr uint32_t kQ4OffEx = kQ4OffQ + kQ4QStages * kQ4QBytes;
+constexpr uint32_t kQ4OffBar = kQ4OffEx + kQ4ExBytes;
+constexpr uint32_t kQ4Bars = 2 * kQ4QStages + 2 * kQ4WStages + 2 * kQ4XMaxStages + 5;
+constexpr size_t kQ4Smem = 1024 + kQ4OffBar + kQ4Bars * 8 + 64;
+static_assert(kQ4Smem <= 232448, "shared memory of the 4-bit GEMM");
+
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// The four epilogue warps agree on a predicate (AND) at barrier 1, so that all of them leave
+// or stay in the unit loop together and the exchange barriers stay matched.
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// four packed bf16x2 words (values 8w' .. 8w'+7 of a row) from one word of nibbles
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t s2, uint32_t b2) {
+  const uint32_t w4 = w >> 4;
+  const uint32_t kMagic = 0x43004300u;              // (128, 128) in bf16
+  const uint32_t kOne = 0x3F803F80u;                // (1, 1)
+  const uint32_t kNeg128 = 0xC300C300u;             // (-128, -128)
+  uint32_t x[4];
+  x[0] = __byte_perm(w, w4, 0x4400);                // nibbles 0 (byte 0) and 1 (byte 2)
+  x[1] = __byte_perm(w, w4, 0x5511);                // nibbles 2, 3
+  x[2] = __byte_perm(w, w4, 0x6622);                // nibbles 4, 5
+  x[3] = __byte_perm(w, w4, 0x7733);                // nibbles 6, 7
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t q128 = (x[j] & 0x000F000Fu) | kMagic;   // 128 + q, exact
+    const uint32_t q = bf2_fma(q128, kOne, kNeg128);        // q, exact
+    o[j] = bf2_fma(s2, q, b2);                              // round(scale * q + bias)
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Epilogue of one 32-token chunk: v[i] = D[row n][token c0 + i].
+template <int EPI>
+__device__ __forceinline__ void q4_epilogue_chunk(const float* v, int n, int n0, int c0, int M,
+                                                  int kb0, int splits, const EpiParams& ep,
+                                                  float* ex) {
+  if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
+    const bool additive = (EPI == EPI_RESID) || ep.accumulate;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int m = c0 + i;
+      if (m >= M) continue;
+      float x = (EPI == EPI_F32) ? v[i] * ep.alpha : v[i];
+      if (EPI == EPI_RESID && ep.ds_map && kb0 == 0) {
+        const int r = ep.ds_map[m];
+        if (r >= 0) x += __bfloat162float(ep.ds[(size_t)r * ep.ldc + n0 + n]);
+      }
+      float* dst = ep.c + (size_t)m * ep.ldc + n0 + n;
+      if (splits > 1)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(x) : "memory");
+      else
+        *dst = additive ? *dst + x : x;
+    }
+  } else {
+    // the partner row (n ^ 64): the other half of a rotation pair, or the up row of a gate
+    epi_bar();                       // the previous chunk's reads are done
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ex[i * kQ4Rows + n] = v[i];
+    epi_bar();
+    const int mlp0 = ep.q_cols + 2 * ep.kv_cols;
+    const int p = n ^ 64;
+    if (n0 < mlp0) {
+      __nv_bfloat16* base = nullptr;
+      __nv_bfloat16* pool = nullptr;
+      int col = n0 + n, kvh = 0;
+      bool rotate = ep.rope != nullptr;
+      if (n0 < ep.q_cols) {
+        base = ep.q_out;
+      } else {
+        const bool is_k = n0 < ep.q_cols + ep.kv_cols;
+        const int off = n0 - ep.q_cols - (is_k ? 0 : ep.kv_cols);
+        kvh = off >> 7;
+        col = off + n;
+        base = is_k ? ep.k_out : ep.v_out;
+        pool = is_k ? ep.k_pool : ep.v_pool;
+        rotate = rotate && is_k;
+      }
+      const int j = n & 63;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int m = c0 + i;
+        if (m >= M) continue;
+        float y = v[i];
+        if (rotate) {
+          // y[j] = x[j] cos - x[j+64] sin ; y[j+64] = x[j+64] cos + x[j] sin  (j < 64)
+          const float2 cs = __ldg(ep.rope + (size_t)m * 64 + j);
+          const float xp = ex[i * kQ4Rows + p];
+          y = n < 64 ? y * cs.x - xp * cs.y : y * cs.x + xp * cs.y;
+        }
+        const __nv_bfloat16 yb = __float2bfloat16_rn(y);
+        if (base) base[(size_t)m * (base == ep.q_out ? ep.ld_q : ep.ld_kv) + col] = yb;
+        if (pool && ep.kv_slot) {
+          const int slot = ep.kv_slot[m];
+          if (slot >= 0) {
+            const int page = slot / ep.page_size, po = slot - page * ep.page_size;
+            pool[(((size_t)page * ep.n_kv + kvh) * ep.page_size + po) * 128 + (n & 127)] = yb;
+          }
+        }
+      }
+    } else if (n < 64) {
+      const int blk = (n0 - mlp0) >> 7;  // 64 intermediate columns per block
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int m = c0 + i;
+        if (m >= M) continue;
+        const float u = ex[i * kQ4Rows + p];
+        ep.act_out[(size_t)m * ep.ld_act + blk * 64 + n] = __float2bfloat16_rn(silu_f(v[i]) * u);
+      }
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kQ4Threads, 1)
+    k_gemm_q4(const __grid_constant__ CUtensorMap tm_x, const uint8_t* __restrict__ wt, int M,
+              int BT, int N, int K, int splits, const EpiParams ep, int* err) {
+  constexpr int QS = kQ4QStages, WS = kQ4WStages;
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQ4OffBar);
+  const uint32_t qfull0 = smem_u32(bars);                      // [QS] words landed (tx)
+  const uint32_t qempty0 = qfull0 + 8 * QS;                    // [QS] read by 8 warps
+  const uint32_t wfull0 = qempty0 + 8 * QS;                    // [WS] tile written (4 warps)
+  const uint32_t wempty0 = wfull0 + 8 * WS;                    // [WS] consumed by the MMAs
+  const uint32_t xfull0 = wempty0 + 8 * WS;                    // [8] token tile landed (tx)
+  const uint32_t xempty0 = xfull0 + 8 * kQ4XMaxStages;         // [8] consumed by the MMAs
+  const uint32_t tfull0 = xempty0 + 8 * kQ4XMaxStages;         // [2]
+  const uint32_t tempty0 = tfull0 + 16;                        // [2]
+  const uint32_t drain = tempty0 + 16;
+  uint32_t* slots = reinterpret_cast<uint32_t*>(bars + kQ4Bars);  // tmem, q / x consumed
+  float* ex = reinterpret_cast<float*>(smem + kQ4OffEx);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int n_tiles = N / kQ4Rows;
+  const int kbt = K / kBK;
+  const int kqt = (kbt + 1) / 2;                   // 128-K blocks (the last may be half)
+  const int units = n_tiles * splits;
+  const uint32_t x_bytes = static_cast<uint32_t>(BT) * 128;
+  int XS = static_cast<int>(kQ4XRing / x_bytes);
+  if (XS > kQ4XMaxStages) XS = kQ4XMaxStages;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < QS; ++i) {
+      mbar_init(qfull0 + 8 * i, 1);
+      mbar_init(qempty0 + 8 * i, 8);
+    }
+    for (int i = 0; i < WS; ++i) {
+      mbar_init(wfull0 + 8 * i, 4);
+      mbar_init(wempty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < kQ4XMaxStages; ++i) {
+      mbar_init(xfull0 + 8 * i, 1);
+      mbar_init(xempty0 + 8 * i, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 128);
+    }
+    mbar_init(drain, 1);
+    slots[1] = 0;
+    slots[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(slots), 256);   // two accumulators, 128 columns apart
+    tmem_relinquish();
+  }
+  if (warp == 14 && lane == 0) tma_prefetch_desc(&tm_x);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = slots[0];
+  pdl_wait();
+
+  int issued = 0;
+  if (warp == 0) {
+    // ------------------------------------------------------------ weight blocks
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
+        const uint8_t* src = wt + ((size_t)t.nt * kqt + t.kb0) * kQ4QBytes;
+        for (int j = t.kb0; j < t.kb1; ++j, src += kQ4QBytes) {
+          if (!(ok = mbar_wait(qempty0 + 8 * stage, phase ^ 1, err))) break;
+          const uint32_t fb = qfull0 + 8 * stage;
+          mbar_expect_tx(fb, kQ4QBytes);
+          bulk_load(sbase + kQ4OffQ + stage * kQ4QBytes, src, kQ4QBytes, fb);
+          ++issued;
+          if (++stage == QS) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------ token tiles
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
+        const int kb_end = min(2 * t.kb1, kbt);
+        for (int kb = 2 * t.kb0; kb < kb_end; ++kb) {
+          if (!(ok = mbar_wait(xempty0 + 8 * stage, phase ^ 1, err))) break;
+          const uint32_t fb = xfull0 + 8 * stage;
+          mbar_expect_tx(fb, x_bytes);
+          tma_load_2d(sbase + kQ4OffX + stage * x_bytes, &tm_x, fb, kb * kBK, 0);
+          ++issued;
+          if (++stage == XS) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kQ4Rows, static_cast<uint32_t>(BT), 0);
+      int xs = 0, ws = 0;
+      uint32_t xph = 0, wph = 0;
+      int iter = 0, consumed = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++iter) {
+        const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
+        const int acc = iter & 1;
+        if (!(ok = mbar_wait(tempty0 + 8 * acc, ((iter >> 1) & 1) ^ 1, err))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * 128;
+        const int kb0 = 2 * t.kb0, kb_end = min(2 * t.kb1, kbt);
+        for (int kb = kb0; kb < kb_end; ++kb) {
+          if (!(ok = mbar_wait(xfull0 + 8 * xs, xph, err))) break;
+          ++consumed;
+          if (!(ok = mbar_wait(wfull0 + 8 * ws, wph, err))) break;
+          tc_fence_after();
+          const uint32_t w0 = sbase + ws * kQ4WBytes;
+          const uint32_t x0 = sbase + kQ4OffX + xs * x_bytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(d_tmem, desc_kmajor_sw128(w0 + 32 * k), desc_kmajor_sw128(x0 + 32 * k), idesc,
+                   (kb > kb0 || k > 0) ? 1u : 0u);
+          tc_commit(xempty0 + 8 * xs);
+          tc_commit(wempty0 + 8 * ws);
+          if (++xs == XS) {
+            xs = 0;
+            xph ^= 1;
+          }
+          if (++ws == WS) {
+            ws = 0;
+            wph ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * acc);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, nullptr);
+      slots[2] = consumed;
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int n = quarter * 32 + lane;               // weight row within the unit
+    int iter = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++iter) {
+      const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
+      const int acc = iter & 1;
+      if (!epi_all(mbar_wait(tfull0 + 8 * acc, (iter >> 1) & 1, err))) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + acc * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
+      for (int c0 = 0; c0 < M; c0 += 32) {
+        float v[32];
+        tmem_ld32(t_row + c0, v);
+        q4_epilogue_chunk<EPI>(v, n, t.nt * kQ4Rows, c0, M, t.kb0, splits, ep, ex);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty0 + 8 * acc);
+    }
+  } else {
+    // ------------------------------------------------------------ dequantisation
+    const int tt = threadIdx.x - 192;
+    const int r = tt & 127, h = tt >> 7;           // row of the W tile, 64-K half of a stage
+    int qs = 0;
+    uint32_t qph = 0;
+    int wcount = 0;                                // W tiles of this CTA so far (all halves)
+    int qconsumed = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
+      for (int j = t.kb0; j < t.kb1; ++j) {
+        const int nkb = (2 * j + 1 < kbt) ? 2 : 1;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qs, qph, err)))) break;
+        const uint32_t qst = sbase + kQ4OffQ + qs * kQ4QBytes;
+        uint32_t sbv = 0, wd[8];
+        if (h < nkb) {
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sbv) : "r"(qst + kQ4QWords + (h * kQ4Rows + r) * 4));
+          // chunk-major block: the 16-byte chunk q of row r at (q * 128 + r) * 16
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(wd[0]), "=r"(wd[1]), "=r"(wd[2]), "=r"(wd[3])
+                       : "r"(qst + ((2 * h) * kQ4Rows + r) * 16));
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(wd[4]), "=r"(wd[5]), "=r"(wd[6]), "=r"(wd[7])
+                       : "r"(qst + ((2 * h + 1) * kQ4Rows + r) * 16));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty0 + 8 * qs);
+        ++qconsumed;
+        if (++qs == QS) {
+          qs = 0;
+          qph ^= 1;
+        }
+        if (h < nkb) {
+          const int wi = wcount + h;
+          const int ws = wi % WS;
+          if (!(ok = __all_sync(0xffffffffu,
+                                mbar_wait(wempty0 + 8 * ws, ((wi / WS) & 1) ^ 1, err))))
+            break;
+          const uint32_t s2 = __byte_perm(sbv, 0, 0x1010);   // (scale, scale)
+          const uint32_t b2 = __byte_perm(sbv, 0, 0x3232);   // (bias, bias)
+          const uint32_t wrow = sbase + ws * kQ4WBytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {              // 16-byte chunk c of the row
+            const uint4 o = dequant_word(wd[c], s2, b2);
+            st_shared_v4(wrow + ((c ^ (r & 7)) << 4), o.x, o.y, o.z, o.w);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(wfull0 + 8 * ws);
+        }
+        wcount += nkb;
+      }
+    }
+    if (tt == 0) slots[1] = qconsumed;
+  }
+  __syncthreads();
+  if (warp == 0 && lane == 0) {
+    // a failed launch may leave loads in flight: wait (bounded) until they have landed
+    for (int i = static_cast<int>(slots[1]); i < issued; ++i)
+      mbar_wait(qfull0 + 8 * (i % QS), (i / QS) & 1, nullptr);
+  }
+  if (warp == 14 && lane == 0) {
+    for (int i = static_cast<int>(slots[2]); i < issued; ++i)
+      mbar_wait(xfull0 + 8 * (i % XS), (i / XS) & 1, nullptr);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 256);
+  }
+}
+
+template <int EPI>
+cc_status launch_q4_t(const CUtensorMap& tx, const uint8_t* wt, int M, int BT, int N, int K,
+                      int splits, const EpiParams& ep, int* err, cudaStream_t s) {
+  static bool attr_set = false;
+  auto kern = k_gemm_q4<EPI>;
+  if (!attr_set) {
+    CC_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kQ4Smem)));
+    attr_set = true;
+  }
+  const int units = (N / kQ4Rows) * splits;
+  const int grid = units < num_sms() ? units : num_sms();
+  CC_CHECK_CUDA(launch_pdl(kern, dim3(grid), dim3(kQ4Threads), kQ4Smem, s, tx, wt, M, BT, N, K,
+                          splits, ep, err));
+  return CC_OK;
+}
+
 }  // namespace
 
 // Tile shape and K splitting. With one row tile (M <= 128: decode steps, the head on a few
@@ -411,6 +837,32 @@ cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N
       case EPI_RESID: return launch_t<128, EPI_RESID>(ta, tb, M, N, K, splits, ep, err, s);
       case EPI_QKV_MLP: return launch_t<128, EPI_QKV_MLP>(ta, tb, M, N, K, 1, ep, err, s);
     }
+  }
+  return CC_ERR_INVALID_ARG;
+}
+
+int gemm_q4_token_tile(int M) { return M <= 16 ? 16 : (M + 15) / 16 * 16; }
+
+cc_status launch_gemm_q4(const CUtensorMap& tx, const void* w_tiled, int M, int N, int K,
+                         int epi, const EpiParams& ep, int* err, cudaStream_t s) {
+  if (M <= 0) return CC_OK;
+  if (M > 128 || N % kQ4Rows != 0 || K % kBK != 0 || !w_tiled ||
+      (reinterpret_cast<uintptr_t>(w_tiled) & 15) != 0)
+    return CC_ERR_INVALID_ARG;
+  const uint8_t* wt = static_cast<const uint8_t*>(w_tiled);
+  const int BT = gemm_q4_token_tile(M);
+  // K splits only for additive epilogues (the f32 one when it accumulates into C), up to one
+  // unit per SM
+  int sp = 1;
+  const int kqt = (K / kBK + 1) / 2;   // 128-K blocks
+  if (epi == EPI_RESID || (epi == EPI_F32 && ep.accumulate)) {
+    const int tiles = N / kQ4Rows;
+    while (tiles * (sp + 1) <= num_sms() && kqt / (sp + 1) >= 2) ++sp;
+  }
+  switch (epi) {
+    case EPI_F32: return launch_q4_t<EPI_F32>(tx, wt, M, BT, N, K, sp, ep, err, s);
+    case EPI_RESID: return launch_q4_t<EPI_RESID>(tx, wt, M, BT, N, K, sp, ep, err, s);
+    case EPI_QKV_MLP: return launch_q4_t<EPI_QKV_MLP>(tx, wt, M, BT, N, K, 1, ep, err, s);
   }
   return CC_ERR_INVALID_ARG;
 }

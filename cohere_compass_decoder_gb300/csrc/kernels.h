@@ -52,6 +52,29 @@ cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N
 // Picks bn / splits for a problem (used by every caller of launch_gemm).
 void gemm_choose(int M, int N, int K, int epi, int* bn, int* splits);
 
+// Tiled 4-bit affine weights of a [rows, K] matrix (rows % 128 == 0, K % 64 == 0): block
+// (t, j), t < rows / 128, j < ceil(K / 128), is kQ4TileBlockBytes contiguous bytes at
+// (t * ceil(K / 128) + j) * kQ4TileBlockBytes holding rows 128 t .. 128 t + 127 and
+// K = 128 j .. 128 j + 127:
+//   bytes [0, 8192)     the rows' packed words (16 per row), chunk-major: the 16-byte chunk
+//                       c (words 4c .. 4c + 3) of row r at (c * 128 + r) * 16
+//   bytes [8192, 9216)  (scale, bias) words of groups 2 j and 2 j + 1: group g, row r at
+//                       (g * 128 + r) * 4, scale's bf16 bits in the low half
+// Words and groups past K are zero.
+constexpr uint32_t kQ4TileBlockBytes = 9216;
+size_t q4_tiled_bytes(int rows, int K);
+// words uint32 [rows, K / 8] (checkpoint order), scales / biases bf16 [rows, K / 64]
+cc_status launch_q4_tile(const uint32_t* words, const uint16_t* scales, const uint16_t* biases,
+                         int rows, int K, uint8_t* out, cudaStream_t s);
+
+// The GEMM with W in 4-bit affine form (group 64 along K), weight-stationary for M <= 128:
+// tx maps the bf16 activations X [M, K] with box 64 x gemm_q4_token_tile(M) rows (128-byte
+// swizzle); w_tiled holds W [N, K] tiled as above (16-byte aligned). N % 128 == 0,
+// K % 64 == 0.
+int gemm_q4_token_tile(int M);
+cc_status launch_gemm_q4(const CUtensorMap& tx, const void* w_tiled, int M, int N, int K,
+                         int epi, const EpiParams& ep, int* err, cudaStream_t s);
+
 // ---------------------------------------------------------------- attention
 // One work item of the prefill attention, for every head group: a 128-query tile and the
 // key tiles [kt0, kt1) it reads. A query tile whose key range is long next to the launch's

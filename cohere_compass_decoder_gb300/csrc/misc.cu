@@ -1,4 +1,5 @@
 // Memory-bound helpers of the path: LayerNorm, the MRoPE cos/sin table, row maps.
+#include <algorithm>
 #include <cmath>
 
 #include "kernels.h"
@@ -256,6 +257,37 @@ __global__ void k_kv_slots_decode(const int32_t* __restrict__ seq_lens, int batc
   n_keys[b] = slot < 0 ? 0 : pos + 1;
 }
 
+
+// The tiled 4-bit weight blocks (layout in kernels.h), one output word per thread-step.
+__global__ void k_q4_tile(const uint32_t* __restrict__ words, const uint16_t* __restrict__ scales,
+                          const uint16_t* __restrict__ biases, int rows, int K,
+                          uint32_t* __restrict__ out) {
+  pdl_wait();
+  const int G = K / 64, W = K / 8, kqt = (G + 1) / 2;
+  constexpr int kWordsPerBlock = kQ4TileBlockBytes / 4;   // 2048 packed + 256 (scale, bias)
+  const size_t total = (size_t)(rows / 128) * kqt * kWordsPerBlock;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t b = i / kWordsPerBlock;
+    const int e = static_cast<int>(i - b * kWordsPerBlock);
+    const int t = static_cast<int>(b / kqt), j = static_cast<int>(b - (size_t)t * kqt);
+    uint32_t v = 0;
+    if (e < 2048) {
+      const int c = e >> 9, r = (e >> 2) & 127, w = 4 * c + (e & 3);
+      const int col = 16 * j + w;
+      if (col < W) v = words[(size_t)(128 * t + r) * W + col];
+    } else {
+      const int g = (e - 2048) >> 7, r = (e - 2048) & 127;
+      const int grp = 2 * j + g;
+      if (grp < G) {
+        const size_t src = (size_t)(128 * t + r) * G + grp;
+        v = static_cast<uint32_t>(scales[src]) | (static_cast<uint32_t>(biases[src]) << 16);
+      }
+    }
+    out[i] = v;
+  }
+}
+
 }  // namespace
 
 cc_status launch_layernorm_bf16(const float* x, const __nv_bfloat16* gamma, __nv_bfloat16* out,
@@ -340,4 +372,19 @@ cc_status launch_kv_slots_decode(const int32_t* seq_lens, int batch, const int32
   return CC_OK;
 }
 
+size_t q4_tiled_bytes(int rows, int K) {
+  return (size_t)(rows / 128) * ((K / 64 + 1) / 2) * kQ4TileBlockBytes;
+}
+
+cc_status launch_q4_tile(const uint32_t* words, const uint16_t* scales, const uint16_t* biases,
+                         int rows, int K, uint8_t* out, cudaStream_t s) {
+  if (rows <= 0 || K <= 0) return CC_OK;
+  const size_t n = q4_tiled_bytes(rows, K) / 4;
+  const int grid = static_cast<int>(std::min<size_t>((n + 255) / 256, 8 * (size_t)num_sms()));
+  CC_CHECK_CUDA(launch_pdl(k_q4_tile, dim3(grid), dim3(256), 0, s, words, scales, biases, rows, K,
+                           reinterpret_cast<uint32_t*>(out)));
+  return CC_OK;
+}
+
 }  // namespace cc
+

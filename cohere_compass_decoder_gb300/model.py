@@ -52,6 +52,40 @@ class DecoderStack:
         self.plan = L.cc_layer_plan_create(self.cfg, list(zip(self.ln, self.w1, self.w2)),
                                            self.final_ln, self.embed)
 
+    def attach_q4(self, layer_q4, embed_q4):
+        """Uploads and tiles the 4-bit affine weights (``layer_q4(i)``: ln and a (words,
+        scales, biases) triple per matrix; ``embed_q4`` one triple) for decode_q4/logits_q4."""
+        H = self.shape.hidden_size
+        u32 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(self.device)
+        tiled = lambda rows, k: torch.empty(L.cc_q4_tiled_bytes(rows, k), dtype=torch.uint8,
+                                            device=self.device)
+        names = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+        self.q4 = []
+        for i in range(self.shape.num_layers):
+            w = layer_q4(i)
+            words = [u32(w[k][0]) for k in names]
+            scales = [to_device(w[k][1], self.device) for k in names]
+            biases = [to_device(w[k][2], self.device) for k in names]
+            w1 = tiled(self.N1, H)
+            w2 = tiled(H, self.K2)
+            L.cc_pack_layer_weights_q4(self.cfg, words, scales, biases, w1, w2)
+            torch.cuda.current_stream().synchronize()
+            self.q4.append((to_device(w["ln"], self.device), w1, w2))
+        ew, es, eb = embed_q4
+        V = ew.shape[0]
+        self.embed_q4 = tiled(V, H)
+        L.cc_pack_q4_tiles(u32(ew), to_device(es, self.device), to_device(eb, self.device), V, H,
+                           self.embed_q4)
+        torch.cuda.current_stream().synchronize()
+        L.cc_layer_plan_attach_q4(self.plan, self.q4, self.embed_q4)
+
+    def decode_q4(self, hidden, pos, seq_lens, page_table, max_pages, kv, stream=None):
+        L.cc_decode_step_q4(self.plan, hidden, pos, seq_lens, page_table, max_pages,
+                            hidden.shape[0], kv, stream)
+
+    def logits_q4(self, hidden, rows, n_rows, out, stream=None):
+        L.cc_logits_q4(self.plan, hidden, rows, n_rows, out, stream)
+
     def prefill(self, hidden, pos, cu_seqlens, n_seqs, ds_rows=None, ds_feats=(), kv=None,
                 page_table=None, max_pages=0, stream=None):
         n_ds_rows = 0 if ds_rows is None else int(ds_rows.numel())

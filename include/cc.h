@@ -31,6 +31,7 @@
 #ifndef CC_H_
 #define CC_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -226,6 +227,67 @@ cc_status cc_decode_step(cc_layer_plan* plan, float* hidden, const int32_t* pos_
 cc_status cc_logits(cc_layer_plan* plan, const float* hidden, const int32_t* rows,
                     int32_t n_rows, float* logits, void* stream);
 
+/* ---------------------------------------------------------------- 4-bit affine weights
+ * The mlx conversion of the checkpoint stores the projections and the embedding in 4-bit
+ * affine form with group size 64 (Compass issue, "Config (config.json)", quantization
+ * {group_size 64, bits 4, mode affine}): w[n, k] = scale[n, k / 64] * q[n, k] +
+ * bias[n, k / 64], q[n, k] the 4-bit field at bit 4 * (k % 8) of the 32-bit word
+ * packed[n, k / 8] (lowest bits first), scale and bias bf16. The decode-step GEMMs below read
+ * these weights directly (about a quarter of the bf16 bytes) and turn each group into bf16
+ * on chip: the dequantised weight is rounded to bf16 (scale * q + bias rounded once), then
+ * multiplied with fp32 accumulation.
+ *
+ * Tiled form (what the GEMMs read): a [rows, K] matrix, rows % 128 == 0, K % 64 == 0, is cut
+ * into blocks of 128 rows x 128 K, block (t, j) at byte (t * ceil(K / 128) + j) * 9216:
+ *   bytes [0, 8192)     the 16 packed words of each of the 128 rows, chunk-major: the
+ *                       16-byte chunk c (words 4c .. 4c + 3 of the row's 16) of row r at
+ *                       byte (c * 128 + r) * 16
+ *   bytes [8192, 9216)  one 32-bit word per group and row, group g (of the block's two) and
+ *                       row r at byte 8192 + (g * 128 + r) * 4: scale's bf16 bits in the low
+ *                       half, bias's in the high half
+ * Words and groups past K are zero. Each block is one contiguous read of the weight stream. */
+typedef struct {
+  const void* ln_w;  /* bf16 [H] LayerNorm gain                                          */
+  const void* w1;    /* tiled [N1, H]: rows arranged as w1 of cc_layer_weights            */
+  const void* w2;    /* tiled [H, K2]: columns arranged as w2                             */
+} cc_layer_weights_q4;
+
+/* Bytes of the tiled form of a [rows, k] matrix (0 unless rows % 128 == 0, k % 64 == 0). */
+size_t cc_q4_tiled_bytes(int32_t rows, int32_t k);
+
+/* Tiles one checkpoint matrix: words uint32 [rows, k / 8], scales and biases bf16
+ * [rows, k / 64] (device) -> out (cc_q4_tiled_bytes(rows, k) bytes, caller-allocated,
+ * 16-byte aligned). rows % 128 == 0 and k % 64 == 0, else CC_ERR_UNSUPPORTED. */
+cc_status cc_pack_q4_tiles(const void* words, const void* scales, const void* biases,
+                           int32_t rows, int32_t k, void* out, void* stream);
+
+/* cc_pack_layer_weights for 4-bit affine matrices: packed[i], scales[i], biases[i] (host
+ * arrays of 7 device pointers, in the order q, k, v, o, gate, up, down) are the checkpoint's
+ * [out, in / 8] uint32 words and [out, in / 64] bf16 scales and biases. Writes w1 and w2 of
+ * cc_layer_weights_q4 (cc_q4_tiled_bytes(N1, H) and cc_q4_tiled_bytes(H, K2) bytes,
+ * caller-allocated) with w1's row and w2's column arrangement. Uses stream-ordered scratch
+ * the size of the larger fused matrix. */
+cc_status cc_pack_layer_weights_q4(const cc_model_config* cfg, const void* const* packed,
+                                   const void* const* scales, const void* const* biases,
+                                   void* w1_out, void* w2_out, void* stream);
+
+/* Gives a bf16 plan the tiled 4-bit affine weights of every layer (layers[num_layers]) and
+ * of the tied embedding (embed_q4: tiled [V, H]) for cc_decode_step_q4 and cc_logits_q4.
+ * Borrowed like the bf16 weights (16-byte aligned). A second call replaces the first. */
+cc_status cc_layer_plan_attach_q4(cc_layer_plan* plan, const cc_layer_weights_q4* layers,
+                                  const void* embed_q4);
+
+/* cc_decode_step with the attached 4-bit weights (same arguments and result up to the
+ * weights' rounding). batch <= 128. CC_ERR_INVALID_ARG when nothing is attached. */
+cc_status cc_decode_step_q4(cc_layer_plan* plan, float* hidden, const int32_t* pos_thw,
+                            const int32_t* seq_lens, const int32_t* page_table,
+                            int32_t max_pages, int32_t batch, const cc_kv_pool* kv,
+                            void* stream);
+
+/* cc_logits with the attached 4-bit embedding as the LM head. n_rows <= 128. */
+cc_status cc_logits_q4(cc_layer_plan* plan, const float* hidden, const int32_t* rows,
+                       int32_t n_rows, float* logits, void* stream);
+
 /* Waits for `stream`, then returns and clears the plan's sticky device error flag
  * (CC_ERR_TIMEOUT / CC_ERR_DEVICE_CHECK), or CC_ERR_CUDA if the stream failed. */
 cc_status cc_sync(cc_layer_plan* plan, void* stream);
@@ -290,6 +352,13 @@ cc_status cc_op_layernorm(const float* x, const void* gamma, void* out, int32_t 
 cc_status cc_op_mrope_table(const int32_t* pos, int32_t tokens, int32_t head_dim,
                             double theta, const int32_t* section_host, float* table,
                             void* stream);
+
+/* The 4-bit affine GEMM of cc_decode_step_q4: C[M, N] = alpha * A[M, K] @ W^T (+ C when
+ * accumulate != 0), W [N, K] in tiled form (cc_pack_q4_tiles), each weight rounded to bf16
+ * after dequantisation. A bf16 [M, K]; C f32 [M, N]. M <= 128, K % 64 == 0, N % 128 == 0;
+ * A and W 16-byte aligned. */
+cc_status cc_op_gemm_q4(const void* a, const void* w_tiled, float* c, int32_t m, int32_t n,
+                        int32_t k, float alpha, int32_t accumulate, void* stream);
 
 /* Dense bf16 GEMM on the tcgen05 tensor cores: C[M, N] = alpha * A[M, K] @ B[N, K]^T
  * (+ C when accumulate != 0). A, B bf16 row-major (K contiguous); C f32 [M, N].

@@ -40,3 +40,28 @@ def run(inp, mirror_bf16=None):
     if inp.wl.mode == "decode":
         return run_decode(inp, True if mirror_bf16 is None else mirror_bf16)
     return run_prefill(inp, mirror_bf16)
+
+
+def dequantized_q4(triple):
+    """A 4-bit affine matrix as the GPU path multiplies it: dequantised exactly, then rounded
+    to bf16 (the reading of the mlx affine weights in a bf16 tensor-core product)."""
+    return O.round_bf16(O.dequantize_affine(*triple))
+
+
+def run_decode_q4(inp, mirror_bf16=True):
+    """run_decode with the workload's 4-bit affine layers and embedding (inp.layer_q4,
+    inp.embed_q4) in place of the bf16 ones."""
+    shape = O.shape_dict(inp.shape)
+
+    def layer(i):
+        q = inp.layer_q4(i)
+        out = {"ln": q["ln"]}
+        for key in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+            out[key] = dequantized_q4(q[key])
+        return out
+
+    h = O.decode_step(inp.hidden, layer, shape, inp.seq_lens, inp.rope_delta, inp.page_table,
+                      inp.kv, inp.wl.page_size, mirror_bf16)
+    embed = dequantized_q4(inp.embed_q4)
+    logits = O.logits(h[inp.head_rows], inp.final_ln, embed, shape, mirror_bf16)
+    return h, logits

@@ -143,6 +143,45 @@ class Inputs:
             self._ds[key] = _draw(rng, (R, self.shape.hidden_size), 0.1, 0.0, self.bf16)
         return self._ds[key]
 
+    # ---- 4-bit affine weights (the mlx conversion's storage form) ------------------------
+    def _affine_q4(self, rng, rows, cols):
+        """(words uint32 [rows, cols / 8], scales, biases bf16 bits [rows, cols / 64]).
+        Words are uniform 32-bit values, so every 4-bit field is uniform on 0..15; scales
+        are (0.02 / 4.6) * U(0.5, 1.5) and biases -7.5 * scale + N(0, 0.002), so a weight
+        spreads about as widely as the N(0, 0.02) bf16 weights."""
+        words = rng.integers(0, 1 << 32, size=(rows, cols // 8), dtype=np.uint64).astype(np.uint32)
+        sc = (np.float32(0.02 / 4.6) * rng.uniform(0.5, 1.5, size=(rows, cols // 64))).astype(np.float32)
+        sc_bits = f32_to_bf16_bits(sc)
+        bias = np.float32(-7.5) * bf16_bits_to_f32(sc_bits) + _draw(rng, sc.shape, 0.002, 0.0, False)
+        return words, sc_bits, f32_to_bf16_bits(bias)
+
+    def layer_q4(self, i: int) -> dict:
+        """Layer i in 4-bit affine form, group 64: ln [H] (bf16 bits, as layer(i)) and, for
+        each of wq, wk, wv, wo, wg, wu, wd, a (words, scales, biases) triple of the same
+        [out, in] matrix shape. Drawn from their own generator (seed, 9, i)."""
+        key = ("q4", i)
+        if key not in self._ds:
+            s = self.shape
+            rng = np.random.default_rng((self.wl.seed, 9, i))
+            H, d, I = s.hidden_size, s.head_dim, s.intermediate_size
+            nq, nkv = s.num_attention_heads, s.num_key_value_heads
+            w = {"ln": self.layer(i)["ln"]}
+            for name, (r, c) in (("wq", (nq * d, H)), ("wk", (nkv * d, H)), ("wv", (nkv * d, H)),
+                                 ("wo", (H, nq * d)), ("wg", (I, H)), ("wu", (I, H)),
+                                 ("wd", (H, I))):
+                w[name] = self._affine_q4(rng, r, c)
+            self._ds[key] = w
+        return self._ds[key]
+
+    @property
+    def embed_q4(self):
+        """The tied embedding [V, H] in 4-bit affine form (seed, 10)."""
+        if "embed_q4" not in self._ds:
+            s = self.shape
+            rng = np.random.default_rng((self.wl.seed, 10))
+            self._ds["embed_q4"] = self._affine_q4(rng, s.vocab_size, s.hidden_size)
+        return self._ds["embed_q4"]
+
     # ---- token-id input (the embedding merge before the path) ----------------------------
     @property
     def token_ids(self) -> np.ndarray:

@@ -129,6 +129,120 @@ def test_gemm_accumulates():
     assert np.abs(f64(c) - want).max() / np.abs(want).max() < 1e-5
 
 
+# --------------------------------------------------------------------------- 4-bit affine GEMM
+def _bits(x):
+    """float values -> bf16 bit patterns (round to nearest even), as the test's own input."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
+
+
+def _u16_dev(u):
+    return torch.from_numpy(np.ascontiguousarray(u).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _u32_dev(u):
+    return torch.from_numpy(np.ascontiguousarray(u, dtype=np.uint32).view(np.int32)).cuda()
+
+
+def _q4_matrix(rng, n, k):
+    """Uniform 4-bit fields; scales of both signs and several binades; biases around
+    -7.5 scale (the mlx conversion's typical offset) plus spread."""
+    words = rng.integers(0, 1 << 32, size=(n, k // 8), dtype=np.uint64).astype(np.uint32)
+    sc = _bits(0.01 * rng.standard_normal((n, k // 64)) * rng.choice([0.25, 1, 4], (n, k // 64)))
+    sf = (sc.astype(np.uint32) << 16).view(np.float32)
+    bi = _bits(-7.5 * sf + 0.01 * rng.standard_normal(sf.shape))
+    return words, sc, bi
+
+
+def _tile_host(words, sc, bi):
+    """The tiled block layout of include/cc.h, written out on the host (a rearrangement)."""
+    rows, W = words.shape
+    G = sc.shape[1]
+    kqt = (G + 1) // 2
+    wpad = np.zeros((rows, kqt * 16), np.uint32)
+    wpad[:, :W] = words
+    sbpad = np.zeros((rows, kqt * 2), np.uint32)
+    sbpad[:, :G] = sc.astype(np.uint32) | (bi.astype(np.uint32) << 16)
+    out = np.zeros((rows // 128, kqt, 2304), np.uint32)
+    for t in range(rows // 128):
+        for j in range(kqt):
+            blk = wpad[128 * t:128 * t + 128, 16 * j:16 * j + 16]          # [row, word]
+            out[t, j, :2048] = blk.reshape(128, 4, 4).transpose(1, 0, 2).reshape(-1)
+            out[t, j, 2048:] = sbpad[128 * t:128 * t + 128, 2 * j:2 * j + 2].T.reshape(-1)
+    return out.reshape(-1)
+
+
+def _q4_upload(words, sc, bi):
+    n, g = sc.shape
+    out = torch.empty(L.cc_q4_tiled_bytes(n, 64 * g), dtype=torch.uint8, device="cuda")
+    L.cc_pack_q4_tiles(_u32_dev(words), _u16_dev(sc), _u16_dev(bi), n, 64 * g, out)
+    return out
+
+
+@pytest.mark.parametrize("rows,k", [(256, 640), (128, 64), (384, 192)])
+def test_q4_tiles_layout(rows, k):
+    rng = np.random.default_rng(rows + k)
+    words = rng.integers(0, 1 << 32, size=(rows, k // 8), dtype=np.uint64).astype(np.uint32)
+    sc = rng.integers(0, 1 << 16, size=(rows, k // 64), dtype=np.uint16)
+    bi = rng.integers(0, 1 << 16, size=(rows, k // 64), dtype=np.uint16)
+    out = _q4_upload(words, sc, bi)
+    _sync()
+    assert out.numel() == (rows // 128) * ((k // 64 + 1) // 2) * 9216
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), _tile_host(words, sc, bi))
+
+
+@pytest.mark.parametrize("m,n,k,acc", [(64, 256, 2048, 0), (1, 128, 64, 0), (128, 384, 640, 0),
+                                       (100, 1280, 1024, 0), (64, 2048, 10240, 1),
+                                       (5, 512, 4096, 1), (16, 256, 192, 0), (64, 256, 1472, 1),
+                                       (33, 128 * 160, 256, 0)])
+def test_gemm_q4_matches_oracle(m, n, k, acc):
+    from oracle.runs import dequantized_q4
+    rng = np.random.default_rng(m + 3 * n + 7 * k)
+    a = bf16_dev(rng.standard_normal((m, k)))
+    words, sc, bi = _q4_matrix(rng, n, k)
+    wt = _q4_upload(words, sc, bi)
+    c0 = rng.standard_normal((m, n)).astype(np.float32)
+    c = torch.from_numpy(c0).cuda() if acc else torch.full((m, n), float("nan"), device="cuda")
+    L.cc_op_gemm_q4(a, wt, c, m, n, k, 0.5, acc)
+    _sync()
+    want = 0.5 * (f64(a) @ dequantized_q4((words, sc, bi)).T) + (c0 if acc else 0.0)
+    got = f64(c)
+    assert np.all(np.isfinite(got))
+    rel = np.abs(got - want).max() / np.abs(want).max()
+    assert rel < 1e-5, rel
+
+
+def test_pack_layer_weights_q4_layout():
+    """w1's rows q | k | v | 64-row gate/up blocks and w2's columns o | down, in tiled form:
+    a byte-exact rearrangement of the seven checkpoint matrices."""
+    from synth import small_shape
+    shape = small_shape(num_layers=1, heads=(4, 2), inter=192)
+    cfg = L.make_config(shape, 16, 16)
+    H, d, I = shape.hidden_size, shape.head_dim, shape.intermediate_size
+    nq, nkv = shape.num_attention_heads, shape.num_key_value_heads
+    dims = [(nq * d, H), (nkv * d, H), (nkv * d, H), (H, nq * d), (I, H), (I, H), (H, I)]
+    rng = np.random.default_rng(5)
+    mats = [(rng.integers(0, 1 << 32, size=(r, c // 8), dtype=np.uint64).astype(np.uint32),
+             rng.integers(0, 1 << 16, size=(r, c // 64), dtype=np.uint16),
+             rng.integers(0, 1 << 16, size=(r, c // 64), dtype=np.uint16)) for r, c in dims]
+    N1, K2 = (nq + 2 * nkv) * d + 2 * I, nq * d + I
+    w1 = torch.empty(L.cc_q4_tiled_bytes(N1, H), dtype=torch.uint8, device="cuda")
+    w2 = torch.empty(L.cc_q4_tiled_bytes(H, K2), dtype=torch.uint8, device="cuda")
+    L.cc_pack_layer_weights_q4(cfg, [_u32_dev(m[0]) for m in mats], [_u16_dev(m[1]) for m in mats],
+                               [_u16_dev(m[2]) for m in mats], w1, w2)
+    _sync()
+
+    def rows_w1(x):
+        q, k_, v, o, g, u, dn = x
+        gu = np.stack([g.reshape(I // 64, 64, -1), u.reshape(I // 64, 64, -1)], 1).reshape(2 * I, -1)
+        return np.concatenate([q, k_, v, gu])
+
+    fused1 = [rows_w1([m[p] for m in mats]) for p in range(3)]
+    fused2 = [np.concatenate([mats[3][p], mats[6][p]], 1) for p in range(3)]
+    assert np.array_equal(w1.cpu().numpy().view(np.uint32), _tile_host(*fused1))
+    assert np.array_equal(w2.cpu().numpy().view(np.uint32), _tile_host(*fused2))
+
+
 # --------------------------------------------------------------------------- prefill attention
 def _attn_case(lens, nq, nkv, window, seed, qscale=1.0, ramp=0.0):
     """ramp > 0 adds a score bias growing with the key index (so the running max keeps

@@ -147,6 +147,26 @@ def test_small_decode_step():
     _check(inp, gw, h, lg)
 
 
+def test_small_decode_step_q4():
+    """The decode step and head on 4-bit affine weights (group 64) against the oracle run on
+    the same weights dequantised and rounded to bf16."""
+    inp = _small_decode(seed=37, B=7)
+    gw = GpuWorkload(inp)
+    gw.stack.attach_q4(inp.layer_q4, inp.embed_q4)
+    h = gw.fresh_hidden()
+    gw.stack.decode_q4(h, gw.pos, gw.seq_lens, gw.page_table, gw.max_pages, gw.kv)
+    n = int(gw.head_rows.numel())
+    lg = torch.empty(n, inp.shape.vocab_size, dtype=torch.float32, device="cuda")
+    gw.stack.logits_q4(h, gw.head_rows, n, lg)
+    gw.sync()
+    h_ref, lg_ref = R.run_decode_q4(inp)
+    assert_close(as_numpy(h), h_ref, TOL_MAX, TOL_MEAN, "hidden")
+    lmx, _ = assert_close(as_numpy(lg), lg_ref, TOL_MAX, TOL_MEAN, "logits")
+    assert lmx / np.abs(lg_ref).max() <= 2e-2
+    # the bf16 and 4-bit weights differ, so must the results
+    assert np.abs(as_numpy(h) - R.run_decode(inp)[0]).max() > 1e-2
+
+
 def test_cfg4_decode_step():
     inp = Inputs(cfg4())
     gw, h, lg = _run(inp)
