@@ -375,34 +375,46 @@ cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
 // along K (the mlx conversion's affine 4-bit weights, Compass issue "Config (config.json)"),
 // for decode-size M <= 128. Weight-stationary: each unit is 128 weight rows (the MMA's M side)
 // against all M tokens (its N side, BT = M rounded up to 16), so the tensor work scales with
-// the batch, and the weights stream from HBM at a quarter of their bf16 size. The weight
-// weights come pre-tiled (launch_q4_tile): the packed words and (scale, bias) words of 128
-// rows x 128 K are one contiguous 9 KB block, fetched with one bulk copy into a deep ring:
-//   warp 0       weight blocks, 12 stages
-//   warp 14      token tiles X (bf16, 128-byte swizzle) per 64-K block, 48 KB ring
-//   warp 1       MMA: 4 x tcgen05.mma (M=128, N=BT, K=16) per 64-K block, D = W X^T in TMEM
-//   warps 2..5   epilogue: TMEM lane = weight row, column = token
-//   warps 6..13  dequantisation: thread (r, h) turns row r of the h-th 64-K half of a packed
-//                stage into bf16 (a 3-stage ring of W tiles); each 32-bit word gives four
-//                bf16x2 pairs: the nibble pair goes into the mantissas of 128.0 (0x4300 | q
-//                is 128 + q in bf16), 128 is subtracted exactly and fma.rn.bf16x2(scale, q,
-//                bias) rounds scale * q + bias once.
-constexpr int kQ4Threads = 480;
+// the batch, and the weights stream from HBM at a quarter of their bf16 size, pre-tiled
+// (launch_q4_tile): the packed words and (scale, bias) words of 128 rows x 128 K are one
+// contiguous 9 KB block. 24 warps:
+//   warp 0       weight blocks: one bulk copy per block into a 12-stage ring
+//   warp 2       token tiles X (bf16, 128-byte swizzle): both 64-K halves of a block per stage
+//   warps 1, 3   MMA, two issuing threads (one when BT > 64) taking alternate blocks into
+//                separate partial accumulators: per block 8 x tcgen05.mma (M=128, N=BT, K=16) with the
+//                dequantised W read from tensor memory (A operand) and X from shared memory.
+//                Each K=16 instruction costs ~96 cycles for any N up to 128 and a barrier
+//                wait a few hundred, so one issuer would leave the tensor core idle while it
+//                waits. The token ring is waited on only here, in order per thread: its
+//                stages may be fewer than the groups, so an out-of-order waiter could mistake
+//                an older phase's parity for its own.
+//   warps 4..7   epilogue: TMEM lane = weight row, column = token
+//   warps 8..23  dequantisation, four groups of four warps (one per TMEM lane quarter); group
+//                g takes every fourth weight block, so four blocks are in flight. Thread r of
+//                a group owns row r: each 32-bit word gives four bf16x2 pairs (the nibble
+//                pair goes into the mantissas of 128.0: 0x4300 | q is 128 + q in bf16; 128 is
+//                subtracted exactly and fma.rn.bf16x2(scale, q, bias) rounds scale * q + bias
+//                once), 32 columns per 64-K half stored to the group's TMEM slot, then the
+//                group marks the block ready.
+// TMEM: accumulators in columns [0, 256): two unit buffers x two partials of 64 columns when
+// BT <= 64 (two MMA issuers), else two unit buffers of 128 (one issuer); W slots (group g,
+// half h) at 256 + 32 (2 g + h).
+constexpr int kQ4Threads = 768;
 constexpr int kQ4Rows = 128;                          // weight rows per unit
-constexpr int kQ4QStages = 12;                        // packed words: 128 K per stage
-constexpr int kQ4WStages = 3;                         // dequantised bf16 tiles: 64 K per stage
-constexpr int kQ4XMaxStages = 8;                      // token tiles: 64 K per stage
+constexpr int kQ4QStages = 12;                        // weight blocks: 128 K per stage
+constexpr int kQ4Groups = 4;                          // dequantisation warp groups
+constexpr int kQ4XMaxStages = 8;                      // token tiles: 128 K per stage
+constexpr int kQ4Chunk = 16;                          // epilogue tokens per TMEM load
 constexpr uint32_t kQ4QWords = kQ4Rows * 64;          // 8 KB: 128 rows x 64 bytes
 constexpr uint32_t kQ4QBytes = kQ4QWords + 2 * kQ4Rows * 4;   // + two groups' (scale, bias)
 static_assert(kQ4QBytes == kQ4TileBlockBytes, "tiled weight block");
-constexpr uint32_t kQ4WBytes = kQ4Rows * kBK * 2;     // 16 KB
-constexpr uint32_t kQ4XRing = 48 * 1024;              // token ring: 48 KB / (BT * 128) stages
-constexpr uint32_t kQ4ExBytes = 32 * kQ4Rows * 4;     // epilogue exchange: 32 tokens x 128 rows
-constexpr uint32_t kQ4OffX = kQ4WStages * kQ4WBytes;
+constexpr uint32_t kQ4XRing = 80 * 1024;              // token ring: 80 KB / (BT * 256) stages
+constexpr uint32_t kQ4ExBytes = kQ4Chunk * kQ4Rows * 4;
+constexpr uint32_t kQ4OffX = 0;
 constexpr uint32_t kQ4OffQ = kQ4OffX + kQ4XRing;
 constexpr uint32_t kQ4OffEx = kQ4OffQ + kQ4QStages * kQ4QBytes;
 constexpr uint32_t kQ4OffBar = kQ4OffEx + kQ4ExBytes;
-constexpr uint32_t kQ4Bars = 2 * kQ4QStages + 2 * kQ4WStages + 2 * kQ4XMaxStages + 5;
+constexpr uint32_t kQ4Bars = 2 * kQ4QStages + 2 * kQ4Groups + 2 * kQ4XMaxStages + 7;
 constexpr size_t kQ4Smem = 1024 + kQ4OffBar + kQ4Bars * 8 + 64;
 static_assert(kQ4Smem <= 232448, "shared memory of the 4-bit GEMM");
 
@@ -431,8 +443,8 @@ __device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
-// four packed bf16x2 words (values 8w' .. 8w'+7 of a row) from one word of nibbles
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t s2, uint32_t b2) {
+// four packed bf16x2 words (values 8 w' .. 8 w' + 7 of a row) from one word of nibbles
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t s2, uint32_t b2, uint32_t* o) {
   const uint32_t w4 = w >> 4;
   const uint32_t kMagic = 0x43004300u;              // (128, 128) in bf16
   const uint32_t kOne = 0x3F803F80u;                // (1, 1)
@@ -442,25 +454,38 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t s2, uint32_t 
   x[1] = __byte_perm(w, w4, 0x5511);                // nibbles 2, 3
   x[2] = __byte_perm(w, w4, 0x6622);                // nibbles 4, 5
   x[3] = __byte_perm(w, w4, 0x7733);                // nibbles 6, 7
-  uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t q128 = (x[j] & 0x000F000Fu) | kMagic;   // 128 + q, exact
     const uint32_t q = bf2_fma(q128, kOne, kNeg128);        // q, exact
     o[j] = bf2_fma(s2, q, b2);                              // round(scale * q + bias)
   }
-  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Epilogue of one 32-token chunk: v[i] = D[row n][token c0 + i].
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Epilogue of one chunk of kQ4Chunk tokens: v[i] = D[row n][token c0 + i].
 template <int EPI>
 __device__ __forceinline__ void q4_epilogue_chunk(const float* v, int n, int n0, int c0, int M,
                                                   int kb0, int splits, const EpiParams& ep,
                                                   float* ex) {
+  constexpr int CH = kQ4Chunk;
   if constexpr (EPI == EPI_F32 || EPI == EPI_RESID) {
     const bool additive = (EPI == EPI_RESID) || ep.accumulate;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < CH; ++i) {
       const int m = c0 + i;
       if (m >= M) continue;
       float x = (EPI == EPI_F32) ? v[i] * ep.alpha : v[i];
@@ -478,14 +503,14 @@ __device__ __forceinline__ void q4_epilogue_chunk(const float* v, int n, int n0,
     // the partner row (n ^ 64): the other half of a rotation pair, or the up row of a gate
     epi_bar();                       // the previous chunk's reads are done
 #pragma unroll
-    for (int i = 0; i < 32; ++i) ex[i * kQ4Rows + n] = v[i];
+    for (int i = 0; i < CH; ++i) ex[i * kQ4Rows + n] = v[i];
     epi_bar();
     const int mlp0 = ep.q_cols + 2 * ep.kv_cols;
     const int p = n ^ 64;
     if (n0 < mlp0) {
       __nv_bfloat16* base = nullptr;
       __nv_bfloat16* pool = nullptr;
-      int col = n0 + n, kvh = 0;
+      int col = n0 + n, kvh = 0, ld = ep.ld_q;
       bool rotate = ep.rope != nullptr;
       if (n0 < ep.q_cols) {
         base = ep.q_out;
@@ -494,13 +519,14 @@ __device__ __forceinline__ void q4_epilogue_chunk(const float* v, int n, int n0,
         const int off = n0 - ep.q_cols - (is_k ? 0 : ep.kv_cols);
         kvh = off >> 7;
         col = off + n;
+        ld = ep.ld_kv;
         base = is_k ? ep.k_out : ep.v_out;
         pool = is_k ? ep.k_pool : ep.v_pool;
         rotate = rotate && is_k;
       }
       const int j = n & 63;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < CH; ++i) {
         const int m = c0 + i;
         if (m >= M) continue;
         float y = v[i];
@@ -511,19 +537,19 @@ __device__ __forceinline__ void q4_epilogue_chunk(const float* v, int n, int n0,
           y = n < 64 ? y * cs.x - xp * cs.y : y * cs.x + xp * cs.y;
         }
         const __nv_bfloat16 yb = __float2bfloat16_rn(y);
-        if (base) base[(size_t)m * (base == ep.q_out ? ep.ld_q : ep.ld_kv) + col] = yb;
+        if (base) base[(size_t)m * ld + col] = yb;
         if (pool && ep.kv_slot) {
           const int slot = ep.kv_slot[m];
           if (slot >= 0) {
             const int page = slot / ep.page_size, po = slot - page * ep.page_size;
-            pool[(((size_t)page * ep.n_kv + kvh) * ep.page_size + po) * 128 + (n & 127)] = yb;
+            pool[(((size_t)page * ep.n_kv + kvh) * ep.page_size + po) * 128 + n] = yb;
           }
         }
       }
     } else if (n < 64) {
       const int blk = (n0 - mlp0) >> 7;  // 64 intermediate columns per block
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < CH; ++i) {
         const int m = c0 + i;
         if (m >= M) continue;
         const float u = ex[i * kQ4Rows + p];
@@ -537,22 +563,22 @@ template <int EPI>
 __global__ void __launch_bounds__(kQ4Threads, 1)
     k_gemm_q4(const __grid_constant__ CUtensorMap tm_x, const uint8_t* __restrict__ wt, int M,
               int BT, int N, int K, int splits, const EpiParams ep, int* err) {
-  constexpr int QS = kQ4QStages, WS = kQ4WStages;
+  constexpr int QS = kQ4QStages;
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kQ4OffBar);
-  const uint32_t qfull0 = smem_u32(bars);                      // [QS] words landed (tx)
-  const uint32_t qempty0 = qfull0 + 8 * QS;                    // [QS] read by 8 warps
-  const uint32_t wfull0 = qempty0 + 8 * QS;                    // [WS] tile written (4 warps)
-  const uint32_t wempty0 = wfull0 + 8 * WS;                    // [WS] consumed by the MMAs
-  const uint32_t xfull0 = wempty0 + 8 * WS;                    // [8] token tile landed (tx)
-  const uint32_t xempty0 = xfull0 + 8 * kQ4XMaxStages;         // [8] consumed by the MMAs
-  const uint32_t tfull0 = xempty0 + 8 * kQ4XMaxStages;         // [2]
-  const uint32_t tempty0 = tfull0 + 16;                        // [2]
-  const uint32_t drain = tempty0 + 16;
+  const uint32_t qfull0 = smem_u32(bars);                      // [QS] block landed (tx)
+  const uint32_t qempty0 = qfull0 + 8 * QS;                    // [QS] read by its group
+  const uint32_t ready0 = qempty0 + 8 * QS;                    // [4] group's block ready
+  const uint32_t wfree0 = ready0 + 8 * kQ4Groups;              // [4] group's slots read
+  const uint32_t xfull0 = wfree0 + 8 * kQ4Groups;              // [8] token tiles landed (tx)
+  const uint32_t xempty0 = xfull0 + 8 * kQ4XMaxStages;         // [8] read by the MMAs
+  const uint32_t tfull0 = xempty0 + 8 * kQ4XMaxStages;         // [2 acc x 2 partials]
+  const uint32_t tempty0 = tfull0 + 32;                        // [2]
+  const uint32_t drain = tempty0 + 16;                         // both MMA threads
   uint32_t* slots = reinterpret_cast<uint32_t*>(bars + kQ4Bars);  // tmem, q / x consumed
   float* ex = reinterpret_cast<float*>(smem + kQ4OffEx);
 
@@ -561,37 +587,42 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
   const int kbt = K / kBK;
   const int kqt = (kbt + 1) / 2;                   // 128-K blocks (the last may be half)
   const int units = n_tiles * splits;
-  const uint32_t x_bytes = static_cast<uint32_t>(BT) * 128;
+  const uint32_t x_half = static_cast<uint32_t>(BT) * 128;   // one 64-K token tile
+  const uint32_t x_bytes = 2 * x_half;
   int XS = static_cast<int>(kQ4XRing / x_bytes);
   if (XS > kQ4XMaxStages) XS = kQ4XMaxStages;
+  // MMA issuers (partials): two while two unit buffers of two partials fit the 256
+  // accumulator columns (BT <= 64), else one; with two, the token ring's stage count is
+  // even so that each stage has one in-order consumer
+  const int npart = BT <= 64 ? 2 : 1;
+  const uint32_t acc_cols = BT <= 64 ? 64u : 128u;
+  if (npart == 2) XS &= ~1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QS; ++i) {
       mbar_init(qfull0 + 8 * i, 1);
-      mbar_init(qempty0 + 8 * i, 8);
+      mbar_init(qempty0 + 8 * i, 4);
     }
-    for (int i = 0; i < WS; ++i) {
-      mbar_init(wfull0 + 8 * i, 4);
-      mbar_init(wempty0 + 8 * i, 1);
+    for (int i = 0; i < kQ4Groups; ++i) {
+      mbar_init(ready0 + 8 * i, 4);
+      mbar_init(wfree0 + 8 * i, 1);
     }
     for (int i = 0; i < kQ4XMaxStages; ++i) {
       mbar_init(xfull0 + 8 * i, 1);
       mbar_init(xempty0 + 8 * i, 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 128);
-    }
-    mbar_init(drain, 1);
+    for (int a = 0; a < 4; ++a) mbar_init(tfull0 + 8 * a, 1);
+    for (int a = 0; a < 2; ++a) mbar_init(tempty0 + 8 * a, 128);
+    mbar_init(drain, 2);
     slots[1] = 0;
     slots[2] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(slots), 256);   // two accumulators, 128 columns apart
+    tmem_alloc(smem_u32(slots), 512);   // accumulators (2 x 128) + W slots (8 x 32)
     tmem_relinquish();
   }
-  if (warp == 14 && lane == 0) tma_prefetch_desc(&tm_x);
+  if (warp == 2 && lane == 0) tma_prefetch_desc(&tm_x);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -621,7 +652,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
         }
       }
     }
-  } else if (warp == 14) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ token tiles
     if (lane == 0) {
       int stage = 0;
@@ -629,12 +660,14 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
-        const int kb_end = min(2 * t.kb1, kbt);
-        for (int kb = 2 * t.kb0; kb < kb_end; ++kb) {
+        for (int j = t.kb0; j < t.kb1; ++j) {
+          const int nkb = (2 * j + 1 < kbt) ? 2 : 1;
           if (!(ok = mbar_wait(xempty0 + 8 * stage, phase ^ 1, err))) break;
           const uint32_t fb = xfull0 + 8 * stage;
-          mbar_expect_tx(fb, x_bytes);
-          tma_load_2d(sbase + kQ4OffX + stage * x_bytes, &tm_x, fb, kb * kBK, 0);
+          mbar_expect_tx(fb, x_half * nkb);
+          for (int h = 0; h < nkb; ++h)
+            tma_load_2d(sbase + kQ4OffX + stage * x_bytes + h * x_half, &tm_x, fb,
+                        (2 * j + h) * kBK, 0);
           ++issued;
           if (++stage == XS) {
             stage = 0;
@@ -643,124 +676,146 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA (two issuers)
+    // Thread p (warp 1: p = 0, warp 3: p = 1) takes the blocks with seq % 2 == p into its
+    // own partial accumulator, so one thread's MMAs run while the other waits. With the
+    // token ring's stage count even, each stage (and each group) has one in-order consumer.
+    const int p = warp >> 1;
+    if (lane == 0 && p < npart) {
       const uint32_t idesc = idesc_bf16(kQ4Rows, static_cast<uint32_t>(BT), 0);
-      int xs = 0, ws = 0;
-      uint32_t xph = 0, wph = 0;
-      int iter = 0, consumed = 0;
+      int xs = p;
+      uint32_t xph = 0;
+      int iter = 0, consumed = 0, seq = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++iter) {
         const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
         const int acc = iter & 1;
         if (!(ok = mbar_wait(tempty0 + 8 * acc, ((iter >> 1) & 1) ^ 1, err))) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * 128;
-        const int kb0 = 2 * t.kb0, kb_end = min(2 * t.kb1, kbt);
-        for (int kb = kb0; kb < kb_end; ++kb) {
+        const uint32_t d_tmem = tmem_base + (acc * npart + p) * acc_cols;
+        bool first = true;
+        for (int j = t.kb0; j < t.kb1 && ok; ++j, ++seq) {
+          if (seq % npart != p) continue;
+          const int nkb = (2 * j + 1 < kbt) ? 2 : 1;
+          const int g = seq % kQ4Groups;
+          // the block's token tiles have landed, and the group's W halves are in TMEM
           if (!(ok = mbar_wait(xfull0 + 8 * xs, xph, err))) break;
           ++consumed;
-          if (!(ok = mbar_wait(wfull0 + 8 * ws, wph, err))) break;
+          if (!(ok = mbar_wait(ready0 + 8 * g, (seq / kQ4Groups) & 1, err))) break;
           tc_fence_after();
-          const uint32_t w0 = sbase + ws * kQ4WBytes;
-          const uint32_t x0 = sbase + kQ4OffX + xs * x_bytes;
+          for (int h = 0; h < nkb; ++h) {
+            const uint32_t a0 = tmem_base + 256 + 32 * (2 * g + h);
+            const uint32_t x0 = sbase + kQ4OffX + xs * x_bytes + h * x_half;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            tc_mma(d_tmem, desc_kmajor_sw128(w0 + 32 * k), desc_kmajor_sw128(x0 + 32 * k), idesc,
-                   (kb > kb0 || k > 0) ? 1u : 0u);
-          tc_commit(xempty0 + 8 * xs);
-          tc_commit(wempty0 + 8 * ws);
-          if (++xs == XS) {
-            xs = 0;
-            xph ^= 1;
+            for (int k = 0; k < kBK / 16; ++k)
+              tc_mma_ts(d_tmem, a0 + 8 * k, desc_kmajor_sw128(x0 + 32 * k), idesc,
+                        (!first || h > 0 || k > 0) ? 1u : 0u);
           }
-          if (++ws == WS) {
-            ws = 0;
-            wph ^= 1;
+          first = false;
+          tc_commit(xempty0 + 8 * xs);
+          tc_commit(wfree0 + 8 * g);
+          xs += npart;                   // this thread's stages: p, p + npart, ...
+          if (xs >= XS) {
+            xs -= XS;
+            xph ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(tfull0 + 8 * acc);
+        tc_commit(tfull0 + 8 * (2 * acc + p));
       }
       tc_commit(drain);
       mbar_wait(drain, 0, nullptr);
-      slots[2] = consumed;
+      atomicAdd(&slots[2], static_cast<uint32_t>(consumed));
     }
-  } else if (warp < 6) {
+    if (lane == 0 && p >= npart) mbar_arrive(drain);   // the idle issuer's share
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;
     const int n = quarter * 32 + lane;               // weight row within the unit
-    int iter = 0;
+    int iter = 0, seq = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++iter) {
       const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
       const int acc = iter & 1;
-      if (!epi_all(mbar_wait(tfull0 + 8 * acc, (iter >> 1) & 1, err))) break;
+      const uint32_t par = (iter >> 1) & 1;
+      // partial p holds data when the unit has a block with seq % npart == p
+      const int nb = t.kb1 - t.kb0;
+      const bool has[2] = {npart == 1 || (seq & 1) == 0 || nb >= 2,
+                           npart == 2 && ((seq & 1) == 1 || nb >= 2)};
+      seq += nb;
+      bool got = mbar_wait(tfull0 + 8 * (2 * acc), par, err);
+      if (npart == 2) got = got && mbar_wait(tfull0 + 8 * (2 * acc + 1), par, err);
+      if (!epi_all(got)) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + acc * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
-      for (int c0 = 0; c0 < M; c0 += 32) {
-        float v[32];
-        tmem_ld32(t_row + c0, v);
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t t0 = tmem_base + lane_off + (acc * npart) * acc_cols;
+      const uint32_t t1 = t0 + acc_cols;
+      for (int c0 = 0; c0 < M; c0 += kQ4Chunk) {
+        float v[kQ4Chunk], w[kQ4Chunk];
+        tmem_ld16((has[0] ? t0 : t1) + c0, v);
+        if (has[0] && has[1]) {
+          tmem_ld16(t1 + c0, w);
+#pragma unroll
+          for (int i = 0; i < kQ4Chunk; ++i) v[i] += w[i];
+        }
         q4_epilogue_chunk<EPI>(v, n, t.nt * kQ4Rows, c0, M, t.kb0, splits, ep, ex);
       }
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
-  } else {
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ dequantisation
-    const int tt = threadIdx.x - 192;
-    const int r = tt & 127, h = tt >> 7;           // row of the W tile, 64-K half of a stage
-    int qs = 0;
-    uint32_t qph = 0;
-    int wcount = 0;                                // W tiles of this CTA so far (all halves)
-    int qconsumed = 0;
+    const int grp = (warp - 8) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;             // row of the unit = TMEM lane
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + 256;
+    int seq = 0, qconsumed = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const Unit t = decode_unit(u, 1, n_tiles, splits, kqt);
-      for (int j = t.kb0; j < t.kb1; ++j) {
+      for (int j = t.kb0; j < t.kb1; ++j, ++seq) {
+        if (seq % kQ4Groups != grp) continue;
         const int nkb = (2 * j + 1 < kbt) ? 2 : 1;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qs, qph, err)))) break;
+        const int qs = seq % QS;
+        const uint32_t use = (seq / kQ4Groups) & 1;   // parity of this group's use
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * qs, (seq / QS) & 1, err))))
+          break;
+        // chunk-major block: the 16-byte chunk c of row r at (c * 128 + r) * 16
         const uint32_t qst = sbase + kQ4OffQ + qs * kQ4QBytes;
-        uint32_t sbv = 0, wd[8];
-        if (h < nkb) {
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(sbv) : "r"(qst + kQ4QWords + (h * kQ4Rows + r) * 4));
-          // chunk-major block: the 16-byte chunk q of row r at (q * 128 + r) * 16
+        uint32_t wd[16], sbv[2];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(wd[0]), "=r"(wd[1]), "=r"(wd[2]), "=r"(wd[3])
-                       : "r"(qst + ((2 * h) * kQ4Rows + r) * 16));
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(wd[4]), "=r"(wd[5]), "=r"(wd[6]), "=r"(wd[7])
-                       : "r"(qst + ((2 * h + 1) * kQ4Rows + r) * 16));
-        }
+                       : "=r"(wd[4 * c]), "=r"(wd[4 * c + 1]), "=r"(wd[4 * c + 2]),
+                         "=r"(wd[4 * c + 3])
+                       : "r"(qst + (c * kQ4Rows + r) * 16));
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          asm volatile("ld.shared.b32 %0, [%1];"
+                       : "=r"(sbv[h])
+                       : "r"(qst + kQ4QWords + (h * kQ4Rows + r) * 4));
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty0 + 8 * qs);
         ++qconsumed;
-        if (++qs == QS) {
-          qs = 0;
-          qph ^= 1;
-        }
-        if (h < nkb) {
-          const int wi = wcount + h;
-          const int ws = wi % WS;
-          if (!(ok = __all_sync(0xffffffffu,
-                                mbar_wait(wempty0 + 8 * ws, ((wi / WS) & 1) ^ 1, err))))
-            break;
-          const uint32_t s2 = __byte_perm(sbv, 0, 0x1010);   // (scale, scale)
-          const uint32_t b2 = __byte_perm(sbv, 0, 0x3232);   // (bias, bias)
-          const uint32_t wrow = sbase + ws * kQ4WBytes + r * 128;
+        // the MMAs of this group's previous block have read its TMEM slots
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(wfree0 + 8 * grp, use ^ 1, err)))) break;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {              // 16-byte chunk c of the row
-            const uint4 o = dequant_word(wd[c], s2, b2);
-            st_shared_v4(wrow + ((c ^ (r & 7)) << 4), o.x, o.y, o.z, o.w);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(wfull0 + 8 * ws);
+        for (int h = 0; h < 2; ++h) {
+          if (h >= nkb) break;
+          const uint32_t s2 = __byte_perm(sbv[h], 0, 0x1010);   // (scale, scale)
+          const uint32_t b2 = __byte_perm(sbv[h], 0, 0x3232);   // (bias, bias)
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) dequant_word(wd[8 * h + c], s2, b2, o + 4 * c);
+          tmem_st32u(t_lane + 32 * (2 * grp + h), o);
         }
-        wcount += nkb;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready0 + 8 * grp);
       }
     }
-    if (tt == 0) slots[1] = qconsumed;
+    if (lane == 0 && quarter == 0) atomicAdd(&slots[1], static_cast<uint32_t>(qconsumed));
   }
   __syncthreads();
   if (warp == 0 && lane == 0) {
@@ -768,14 +823,14 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     for (int i = static_cast<int>(slots[1]); i < issued; ++i)
       mbar_wait(qfull0 + 8 * (i % QS), (i / QS) & 1, nullptr);
   }
-  if (warp == 14 && lane == 0) {
+  if (warp == 2 && lane == 0) {
     for (int i = static_cast<int>(slots[2]); i < issued; ++i)
       mbar_wait(xfull0 + 8 * (i % XS), (i / XS) & 1, nullptr);
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 256);
+    tmem_dealloc(tmem_base, 512);
   }
 }
 

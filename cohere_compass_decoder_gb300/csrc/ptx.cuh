@@ -54,6 +54,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase of parity `parity`; its result can be consumed well after
+// it is issued, so a thread can overlap the test with other work.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase of parity `parity` of the barrier has completed. Gives up, sets
 // *err = CC_DEV_TIMEOUT and returns false after about kWaitTimeoutCycles SM clocks, or
 // returns false early when *err is already set (another warp or an earlier launch gave

@@ -194,7 +194,8 @@ def test_q4_tiles_layout(rows, k):
 @pytest.mark.parametrize("m,n,k,acc", [(64, 256, 2048, 0), (1, 128, 64, 0), (128, 384, 640, 0),
                                        (100, 1280, 1024, 0), (64, 2048, 10240, 1),
                                        (5, 512, 4096, 1), (16, 256, 192, 0), (64, 256, 1472, 1),
-                                       (33, 128 * 160, 256, 0)])
+                                       (33, 128 * 160, 256, 0), (128, 128 * 400, 384, 0),
+                                       (100, 128 * 320, 640, 0)])
 def test_gemm_q4_matches_oracle(m, n, k, acc):
     from oracle.runs import dequantized_q4
     rng = np.random.default_rng(m + 3 * n + 7 * k)
