@@ -525,23 +525,34 @@ __device__ __forceinline__ void q4_epilogue_chunk(const float* v, int n, int n0,
         rotate = rotate && is_k;
       }
       const int j = n & 63;
+      const bool to_pool = pool && ep.kv_slot;
+      // per 8 tokens: every load first (cos / sin, cache slots), then the stores, so that
+      // the loads' latency is paid once per 8 tokens, not once per token behind the stores
+      constexpr int SB = 8;
 #pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        const int m = c0 + i;
-        if (m >= M) continue;
-        float y = v[i];
-        if (rotate) {
-          // y[j] = x[j] cos - x[j+64] sin ; y[j+64] = x[j+64] cos + x[j] sin  (j < 64)
-          const float2 cs = __ldg(ep.rope + (size_t)m * 64 + j);
-          const float xp = ex[i * kQ4Rows + p];
-          y = n < 64 ? y * cs.x - xp * cs.y : y * cs.x + xp * cs.y;
+      for (int i0 = 0; i0 < CH; i0 += SB) {
+        float2 cs[SB];
+        int slot[SB];
+#pragma unroll
+        for (int i = 0; i < SB; ++i) {
+          const int m = c0 + i0 + i;
+          cs[i] = (rotate && m < M) ? __ldg(ep.rope + (size_t)m * 64 + j) : make_float2(1.f, 0.f);
+          slot[i] = (to_pool && m < M) ? __ldg(ep.kv_slot + m) : -1;
         }
-        const __nv_bfloat16 yb = __float2bfloat16_rn(y);
-        if (base) base[(size_t)m * ld + col] = yb;
-        if (pool && ep.kv_slot) {
-          const int slot = ep.kv_slot[m];
-          if (slot >= 0) {
-            const int page = slot / ep.page_size, po = slot - page * ep.page_size;
+#pragma unroll
+        for (int i = 0; i < SB; ++i) {
+          const int m = c0 + i0 + i;
+          if (m >= M) continue;
+          float y = v[i0 + i];
+          if (rotate) {
+            // y[j] = x[j] cos - x[j+64] sin ; y[j+64] = x[j+64] cos + x[j] sin  (j < 64)
+            const float xp = ex[(i0 + i) * kQ4Rows + p];
+            y = n < 64 ? y * cs[i].x - xp * cs[i].y : y * cs[i].x + xp * cs[i].y;
+          }
+          const __nv_bfloat16 yb = __float2bfloat16_rn(y);
+          if (base) base[(size_t)m * ld + col] = yb;
+          if (slot[i] >= 0) {
+            const int page = slot[i] / ep.page_size, po = slot[i] - page * ep.page_size;
             pool[(((size_t)page * ep.n_kv + kvh) * ep.page_size + po) * 128 + n] = yb;
           }
         }
