@@ -139,17 +139,41 @@ def mrope_axis(half: int, section):
     return ax
 
 
-def mrope_cos_sin(pos, head_dim: int, theta: float, section):
+def mrope_sections_hwt(half: int, section):
+    """The contiguous-section layout ([Compass issue], "Acceptance criteria", the correction
+    to the RoPE item: the checkpoint's rotary class pre-permutes inv_freq and gives the axes
+    contiguous [H, W, T] sections). The pages name the layout but not the permutation. Reading
+    (parity unpinned): the rotary index k runs first over the frequencies the interleaved rule
+    sends to h, in increasing frequency index, then over those it sends to w, then over those
+    it sends to t -- the same (axis, frequency) pairs as the interleaved layout, in contiguous
+    sections of sizes section[1], section[2], section[0].
+    Returns (axis[k], freq_index[k]) for k < half."""
+    ax_int = mrope_axis(half, section)
+    order = [j for a in (1, 2, 0) for j in range(half) if ax_int[j] == a]
+    return ax_int[order], np.asarray(order, dtype=np.int64)
+
+
+MROPE_LAYOUTS = ("interleaved", "sections_hwt")
+
+
+def mrope_cos_sin(pos, head_dim: int, theta: float, section, layout: str = "interleaved"):
     """cos, sin of shape [T, head_dim]: inv_freq[j] = theta**(-2j/head_dim),
-    freqs[:, j] = pos[axis(j)] * inv_freq[j], then cos/sin of concat(freqs, freqs)."""
+    freqs[:, k] = pos[axis(k)] * inv_freq[f(k)], then cos/sin of concat(freqs, freqs).
+    layout "interleaved" (the contract): axis(k) = mrope_axis, f(k) = k; "sections_hwt":
+    mrope_sections_hwt."""
     half = head_dim // 2
     j = np.arange(half, dtype=np.float64)
     inv_freq = float(theta) ** (-2.0 * j / head_dim)
-    ax = mrope_axis(half, section)
+    if layout == "interleaved":
+        ax, fidx = mrope_axis(half, section), np.arange(half)
+    elif layout == "sections_hwt":
+        ax, fidx = mrope_sections_hwt(half, section)
+    else:
+        raise ValueError(f"unknown MRoPE layout {layout!r}")
     pos = np.asarray(pos, dtype=np.float64)
     freqs = np.empty((pos.shape[1], half), dtype=np.float64)
     for jj in range(half):
-        freqs[:, jj] = pos[ax[jj]] * inv_freq[jj]
+        freqs[:, jj] = pos[ax[jj]] * inv_freq[fidx[jj]]
     emb = np.concatenate([freqs, freqs], axis=1)
     return np.cos(emb), np.sin(emb)
 
@@ -321,7 +345,8 @@ def prefill(hidden, layers, shape, pos, cu_seqlens, ds_rows=None, ds=(), mirror_
     i -> layer dict), ``pos`` the [3, T] position ids.
     """
     h = np.array(hidden, dtype=np.float64)
-    cos_sin = mrope_cos_sin(pos, shape["head_dim"], shape["rope_theta"], shape["mrope_section"])
+    cos_sin = mrope_cos_sin(pos, shape["head_dim"], shape["rope_theta"], shape["mrope_section"],
+                            shape["mrope_layout"])
     get = layers if callable(layers) else (lambda i: layers[i])
     hs = []
     for i in range(shape["num_layers"]):
@@ -361,7 +386,8 @@ def decode_step(hidden, layers, shape, seq_lens, rope_delta, page_table, kv, pag
     B = h.shape[0]
     nq, nkv, d = shape["num_attention_heads"], shape["num_key_value_heads"], shape["head_dim"]
     pos = decode_positions(seq_lens, rope_delta)
-    cos, sin = mrope_cos_sin(pos, d, shape["rope_theta"], shape["mrope_section"])
+    cos, sin = mrope_cos_sin(pos, d, shape["rope_theta"], shape["mrope_section"],
+                             shape["mrope_layout"])
     get = layers if callable(layers) else (lambda i: layers[i])
     for li in range(shape["num_layers"]):
         layer = get(li)
@@ -399,9 +425,11 @@ def shape_dict(shape) -> dict:
     keys = ["num_layers", "hidden_size", "num_attention_heads", "num_key_value_heads",
             "head_dim", "intermediate_size", "vocab_size", "sliding_window", "mrope_section",
             "rope_theta", "layer_types", "layer_norm_eps", "logit_scale"]
-    if isinstance(shape, dict):
-        return {k: shape[k] for k in keys}
-    return {k: getattr(shape, k) for k in keys}
+    get = (lambda k, d=None: shape.get(k, d)) if isinstance(shape, dict) else \
+        (lambda k, d=None: getattr(shape, k, d))
+    out = {k: get(k) for k in keys}
+    out["mrope_layout"] = get("mrope_layout", "interleaved")
+    return out
 
 
 __all__ = [n for n in dir() if not n.startswith("_") and n != "np"]

@@ -35,6 +35,7 @@ class ModelShape:
     layer_norm_eps: float = 1e-5
     logit_scale: float = 0.0625
     dtype: str = "bf16"  # "bf16" or "f32": storage type of weights and activations
+    mrope_layout: str = "interleaved"  # or "sections_hwt" (contiguous [H, W, T] sections)
 
     def __post_init__(self):
         assert len(self.layer_types) == self.num_layers
@@ -159,7 +160,7 @@ CONFIGS = {1: cfg1, 2: cfg2, 3: cfg3, 4: cfg4, 5: cfg5}
 
 def small_shape(num_layers=2, layer_types=None, window=64, dtype="bf16", hidden=256,
                 heads=(4, 2), head_dim=128, inter=384, vocab=640, section=None,
-                theta=50000.0, logit_scale=0.0625) -> ModelShape:
+                theta=50000.0, logit_scale=0.0625, mrope_layout="interleaved") -> ModelShape:
     """A reduced model for parity tests; head_dim stays 128 unless asked otherwise."""
     if layer_types is None:
         layer_types = tuple(FULL if i % 4 == 3 else SLIDING for i in range(num_layers))
@@ -171,4 +172,4 @@ def small_shape(num_layers=2, layer_types=None, window=64, dtype="bf16", hidden=
                       num_key_value_heads=heads[1], head_dim=head_dim, intermediate_size=inter,
                       vocab_size=vocab, sliding_window=window, mrope_section=tuple(section),
                       rope_theta=theta, layer_types=tuple(layer_types), dtype=dtype,
-                      logit_scale=logit_scale)
+                      logit_scale=logit_scale, mrope_layout=mrope_layout)

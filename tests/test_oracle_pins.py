@@ -104,6 +104,48 @@ def test_mrope_reads_the_selected_axis():
             assert math.isclose(sin[0, j + 64], math.sin(ang), abs_tol=1e-9)
 
 
+def test_sections_layout_is_contiguous_hwt():
+    """The corrected layout's structure ([Compass issue] "Acceptance criteria": contiguous
+    [H, W, T] sections): the first section[1] rotary indices read h, the next section[2] w,
+    the remaining section[0] t."""
+    for section in [(24, 20, 20), (12, 10, 10), (16, 8, 8)]:
+        half = sum(section)
+        ax, _ = O.mrope_sections_hwt(half, section)
+        want = [1] * section[1] + [2] * section[2] + [0] * section[0]
+        assert ax.tolist() == want
+
+
+def test_sections_layout_reads_the_page_frequencies_per_axis():
+    """Reading of the pre-permuted inv_freq: each section takes, in increasing order, the
+    frequency indices the page's interleaved rule gives to its axis (the page's lists)."""
+    g = read_golden("mrope_selector_section_24_20_20.txt")
+    ax, fidx = O.mrope_sections_hwt(64, (24, 20, 20))
+    assert fidx.tolist() == g["h"] + g["w"] + g["t"]
+    pos = np.array([[7], [1000], [123456]])
+    cos, sin = O.mrope_cos_sin(pos, 128, 50000.0, (24, 20, 20), "sections_hwt")
+    k = 0
+    for axis, name in [(1, "h"), (2, "w"), (0, "t")]:
+        for j in g[name]:
+            ang = pos[axis, 0] * 50000.0 ** (-j / 64.0)
+            assert math.isclose(cos[0, k], math.cos(ang), abs_tol=1e-9)
+            assert math.isclose(sin[0, k + 64], math.sin(ang), abs_tol=1e-9)
+            k += 1
+    assert k == 64
+
+
+def test_sections_layout_is_a_permutation_of_the_interleaved_pairs():
+    """Both layouts rotate by the same (axis, frequency) pairs: on any positions the columns of
+    one cos/sin table are a permutation of the other's."""
+    rng = np.random.default_rng(4)
+    pos = rng.integers(0, 9000, size=(3, 23))
+    ci, si = O.mrope_cos_sin(pos, 128, 50000.0, (24, 20, 20))
+    cs, ss = O.mrope_cos_sin(pos, 128, 50000.0, (24, 20, 20), "sections_hwt")
+    _, fidx = O.mrope_sections_hwt(64, (24, 20, 20))
+    np.testing.assert_array_equal(cs[:, :64], ci[:, fidx])
+    np.testing.assert_array_equal(ss[:, 64:], si[:, 64 + fidx])
+    assert not np.allclose(cs, ci)
+
+
 def test_rope_preserves_pair_norms():
     rng = np.random.default_rng(2)
     pos = rng.integers(0, 5000, size=(3, 50))
