@@ -16,6 +16,7 @@ CC_OK, CC_ERR_INVALID_ARG, CC_ERR_UNSUPPORTED, CC_ERR_OOM, CC_ERR_CUDA, CC_ERR_T
     CC_ERR_DEVICE_CHECK = range(7)
 CC_SLIDING, CC_FULL = 0, 1
 CC_F32, CC_BF16 = 0, 1
+MROPE_LAYOUTS = ("interleaved", "sections_hwt")      # cc_mrope_layout values 0, 1
 
 EXPORTS = [
     "cc_status_string", "cc_build_mrope_positions", "cc_build_decode_positions",
@@ -26,7 +27,7 @@ EXPORTS = [
     "cc_kernel_class_name", "cc_op_attention_decode_noalloc", "cc_prefill_forward_tokens",
     "cc_op_embed_merge", "cc_prefill_forward_chunk", "cc_q4_tiled_bytes", "cc_pack_q4_tiles",
     "cc_pack_layer_weights_q4", "cc_layer_plan_attach_q4", "cc_decode_step_q4", "cc_logits_q4",
-    "cc_op_gemm_q4",
+    "cc_op_gemm_q4", "cc_op_mrope_table_layout",
 ]
 KERNEL_CLASSES = ["rope_table", "row_maps", "layernorm", "gemm_qkv_mlp", "attn_prefill",
                   "gemm_out_resid", "attn_decode", "gemm_head", "f32_path", "embed_merge"]
@@ -46,7 +47,8 @@ class cc_model_config(C.Structure):
                 ("mrope_section", C.c_int32 * 3), ("kv_page_size", C.c_int32),
                 ("max_tokens", C.c_int32), ("dtype", C.c_int32),
                 ("layer_types", C.POINTER(C.c_int32)), ("rope_theta", C.c_double),
-                ("layer_norm_eps", C.c_float), ("logit_scale", C.c_float)]
+                ("layer_norm_eps", C.c_float), ("logit_scale", C.c_float),
+                ("mrope_layout", C.c_int32)]
 
 
 class cc_layer_weights(C.Structure):
@@ -117,6 +119,7 @@ def lib() -> C.CDLL:
             "cc_op_embed_merge": (C.c_int, [vp, i32, vp, i32, i32, vp, vp, i32, vp, vp, C.c_float,
                                             vp, vp]),
             "cc_op_mrope_table": (C.c_int, [vp, i32, i32, C.c_double, p32, vp, vp]),
+            "cc_op_mrope_table_layout": (C.c_int, [vp, i32, i32, C.c_double, p32, i32, vp, vp]),
             "cc_op_gemm_bf16": (C.c_int, [vp, vp, vp, i32, i32, i32, C.c_float, i32, vp]),
             "cc_op_attention_prefill": (C.c_int, [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                                   i32, vp]),
@@ -219,6 +222,7 @@ def make_config(shape, max_tokens, page_size=16):
     cfg.rope_theta = float(shape.rope_theta)
     cfg.layer_norm_eps = float(shape.layer_norm_eps)
     cfg.logit_scale = float(shape.logit_scale)
+    cfg.mrope_layout = MROPE_LAYOUTS.index(getattr(shape, "mrope_layout", "interleaved"))
     cfg._keep = types
     return cfg
 
@@ -356,6 +360,13 @@ def cc_op_layernorm(x, gamma, out, rows, hidden, eps, row_idx=None, stream=None)
 def cc_op_mrope_table(pos, tokens, head_dim, theta, section, table, stream=None):
     _check(lib().cc_op_mrope_table(_ptr(pos), tokens, head_dim, float(theta), _i32_array(section),
                                    _ptr(table), _stream(stream)), "cc_op_mrope_table")
+
+
+def cc_op_mrope_table_layout(pos, tokens, head_dim, theta, section, layout, table, stream=None):
+    _check(lib().cc_op_mrope_table_layout(_ptr(pos), tokens, head_dim, float(theta),
+                                          _i32_array(section), MROPE_LAYOUTS.index(layout),
+                                          _ptr(table), _stream(stream)),
+           "cc_op_mrope_table_layout")
 
 
 def cc_op_gemm_bf16(a, b, c, m, n, k, alpha=1.0, accumulate=0, stream=None):

@@ -227,6 +227,8 @@ static cc_status check_config(const cc_model_config* c) {
       c->mrope_section[0] + c->mrope_section[1] + c->mrope_section[2] != c->head_dim / 2)
     return CC_ERR_INVALID_ARG;
   if (c->dtype != CC_BF16 && c->dtype != CC_F32) return CC_ERR_INVALID_ARG;
+  if (c->mrope_layout != CC_MROPE_INTERLEAVED && c->mrope_layout != CC_MROPE_SECTIONS_HWT)
+    return CC_ERR_INVALID_ARG;
   if (!(c->rope_theta > 0.0) || !(c->layer_norm_eps >= 0.f)) return CC_ERR_INVALID_ARG;
   for (int i = 0; i < c->num_layers; ++i)
     if (c->layer_types[i] != CC_SLIDING && c->layer_types[i] != CC_FULL) return CC_ERR_INVALID_ARG;
@@ -524,7 +526,7 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
                              hidden, static_cast<const __nv_bfloat16*>(p->layers[0].ln_w),
                              c.layer_norm_eps, p->a, p->err, s));
   }
-  CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos, T, p->d, c.rope_theta, c.mrope_section, p->rope, s));
+  CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos, T, p->d, c.rope_theta, c.mrope_section, c.mrope_layout, p->rope, s));
   if (n_ds > 0) CC_TIMED(p, CC_K_ROW_MAPS, s, launch_ds_map(ds_rows, n_ds_rows, T, p->ds_map, p->err, s));
   if (kv)
     CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_prefill(cu, n_seqs, T, page_table, max_pages, c.kv_page_size,
@@ -605,7 +607,7 @@ static cc_status prefill_f32(cc_layer_plan* p, float* hidden, const int32_t* pos
                              int n_seqs, int T, const int32_t* ds_rows, int n_ds_rows,
                              const void* const* ds_feats, int n_ds, cudaStream_t s) {
   const cc_model_config& c = p->cfg;
-  CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos, T, p->d, c.rope_theta, c.mrope_section, p->rope, s));
+  CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos, T, p->d, c.rope_theta, c.mrope_section, c.mrope_layout, p->rope, s));
   for (int i = 0; i < c.num_layers; ++i) {
     const bool sliding = p->types[i] == CC_SLIDING;
     CC_TIMED(p, CC_K_F32_PATH, s, launch_layernorm_f32(hidden, static_cast<const float*>(p->layers[i].ln_w), p->af,
@@ -750,7 +752,7 @@ static cc_status decode_step(cc_layer_plan* p, float* hidden, const int32_t* pos
   scr.part_o = p->dec_scratch;
   scr.part_ml = p->dec_scratch + (size_t)batch * p->nq * decode_splits(max_pages) * 128;
 
-  CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos_thw, batch, p->d, c.rope_theta, c.mrope_section, p->rope, s));
+  CC_TIMED(p, CC_K_ROPE_TABLE, s, launch_mrope_table(pos_thw, batch, p->d, c.rope_theta, c.mrope_section, c.mrope_layout, p->rope, s));
   CC_TIMED(p, CC_K_ROW_MAPS, s, launch_kv_slots_decode(seq_lens, batch, page_table, max_pages, c.kv_page_size,
                                          kv->n_pages, p->kv_slot, p->n_keys, p->err, s));
   CUtensorMap ta, ta2;
@@ -911,16 +913,27 @@ extern "C" cc_status cc_op_embed_merge(const int32_t* token_ids, int32_t tokens,
   return st;
 }
 
+extern "C" cc_status cc_op_mrope_table_layout(const int32_t* pos, int32_t tokens,
+                                              int32_t head_dim, double theta,
+                                              const int32_t* section_host, int32_t layout,
+                                              float* table, void* stream) {
+  if (tokens < 0 || head_dim <= 0 || head_dim % 2 || !section_host || !(theta > 0))
+    return CC_ERR_INVALID_ARG;
+  if (section_host[0] < 0 || section_host[1] < 0 || section_host[2] < 0 ||
+      section_host[0] + section_host[1] + section_host[2] != head_dim / 2)
+    return CC_ERR_INVALID_ARG;
+  if (layout != CC_MROPE_INTERLEAVED && layout != CC_MROPE_SECTIONS_HWT) return CC_ERR_INVALID_ARG;
+  if (tokens == 0) return CC_OK;
+  if (!pos || !table) return CC_ERR_INVALID_ARG;
+  return launch_mrope_table(pos, tokens, head_dim, theta, section_host, layout,
+                            reinterpret_cast<float2*>(table), static_cast<cudaStream_t>(stream));
+}
+
 extern "C" cc_status cc_op_mrope_table(const int32_t* pos, int32_t tokens, int32_t head_dim,
                                        double theta, const int32_t* section_host, float* table,
                                        void* stream) {
-  if (tokens < 0 || head_dim <= 0 || head_dim % 2 || !section_host || !(theta > 0))
-    return CC_ERR_INVALID_ARG;
-  if (section_host[0] + section_host[1] + section_host[2] != head_dim / 2) return CC_ERR_INVALID_ARG;
-  if (tokens == 0) return CC_OK;
-  if (!pos || !table) return CC_ERR_INVALID_ARG;
-  return launch_mrope_table(pos, tokens, head_dim, theta, section_host,
-                            reinterpret_cast<float2*>(table), static_cast<cudaStream_t>(stream));
+  return cc_op_mrope_table_layout(pos, tokens, head_dim, theta, section_host,
+                                  CC_MROPE_INTERLEAVED, table, stream);
 }
 
 extern "C" cc_status cc_op_gemm_bf16(const void* a, const void* b, float* c, int32_t m, int32_t n,

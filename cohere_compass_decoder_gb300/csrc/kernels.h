@@ -165,7 +165,7 @@ cc_status launch_layernorm_bf16(const float* x, const __nv_bfloat16* gamma, __nv
 cc_status launch_layernorm_f32(const float* x, const float* gamma, float* out, int rows, int H,
                                float eps, const int32_t* row_idx, cudaStream_t s);
 cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double theta,
-                             const int32_t section[3], float2* table, cudaStream_t s);
+                             const int32_t section[3], int layout, float2* table, cudaStream_t s);
 // h[row] = f32(mm_embeds[mm_map[row]]) when mm_map[row] >= 0, else f32(embed[tok[row]]);
 // ln_out (nullable) = bf16(LayerNorm(h row) * ln_w). Out-of-range token ids set err.
 cc_status launch_embed_ln(const int32_t* tok, const __nv_bfloat16* embed, int V,

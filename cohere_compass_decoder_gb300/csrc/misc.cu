@@ -153,21 +153,20 @@ cc_status launch_ln(const float* x, const void* gamma, OutT* out, int rows, int 
 // angle = pos[axis] * theta^(-2j/d). theta^(-2j/d) is evaluated once per call on the host
 // in double precision; the angle (up to ~1e5 rad) is formed and reduced modulo 2*pi in
 // double precision; sincosf then sees |r| <= pi.
-struct InvFreq {
+// per rotary index k: the position axis it reads and its inverse frequency
+struct MropeTbl {
   double v[64];
+  int32_t axis[64];
 };
 
-__global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, const InvFreq f,
-                              int sec_h, int sec_w, float2* __restrict__ table) {
+__global__ void k_mrope_table(const int32_t* __restrict__ pos, int T, int half, const MropeTbl f,
+                              float2* __restrict__ table) {
   pdl_trigger();
   pdl_wait();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= T * half) return;
   const int t = idx / half, j = idx - t * half;
-  int axis = 0;
-  if (j % 3 == 1 && j < 3 * sec_h) axis = 1;
-  else if (j % 3 == 2 && j < 3 * sec_w) axis = 2;
-  const double ang = static_cast<double>(pos[axis * T + t]) * f.v[j];
+  const double ang = static_cast<double>(pos[f.axis[j] * T + t]) * f.v[j];
   const double two_pi = 6.283185307179586476925286766559;
   const double inv_two_pi = 0.15915494309189533576888376337251;
   const double r = fma(-two_pi, rint(ang * inv_two_pi), ang);
@@ -325,15 +324,37 @@ cc_status launch_embed_ln(const int32_t* tok, const __nv_bfloat16* embed, int V,
 }
 
 cc_status launch_mrope_table(const int32_t* pos, int T, int head_dim, double theta,
-                             const int32_t section[3], float2* table, cudaStream_t s) {
+                             const int32_t section[3], int layout, float2* table, cudaStream_t s) {
   if (T <= 0) return CC_OK;
   const int half = head_dim / 2;
   if (half > 64) return CC_ERR_UNSUPPORTED;
-  InvFreq f{};
-  for (int j = 0; j < half; ++j) f.v[j] = std::pow(theta, -2.0 * j / head_dim);
+  if (layout != CC_MROPE_INTERLEAVED && layout != CC_MROPE_SECTIONS_HWT) return CC_ERR_INVALID_ARG;
+  // the interleaved assignment: index j reads h when j % 3 == 1 and j < 3 section[1], w when
+  // j % 3 == 2 and j < 3 section[2], else t, at frequency j
+  int axis_il[64];
+  for (int j = 0; j < half; ++j)
+    axis_il[j] = (j % 3 == 1 && j < 3 * section[1]) ? 1 : (j % 3 == 2 && j < 3 * section[2]) ? 2 : 0;
+  MropeTbl f{};
+  if (layout == CC_MROPE_INTERLEAVED) {
+    for (int j = 0; j < half; ++j) {
+      f.axis[j] = axis_il[j];
+      f.v[j] = std::pow(theta, -2.0 * j / head_dim);
+    }
+  } else {
+    // contiguous sections h, w, t, each holding its axis's frequencies in increasing order
+    int k = 0;
+    const int order[3] = {1, 2, 0};
+    for (int a : order)
+      for (int j = 0; j < half; ++j)
+        if (axis_il[j] == a) {
+          f.axis[k] = a;
+          f.v[k] = std::pow(theta, -2.0 * j / head_dim);
+          ++k;
+        }
+  }
   const int n = T * half;
   CC_CHECK_CUDA(launch_pdl(k_mrope_table, dim3((n + 255) / 256), dim3(256), 0, s, pos, T, half, f,
-                            section[1], section[2], table));
+                            table));
   return CC_OK;
 }
 

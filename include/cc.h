@@ -51,6 +51,18 @@ typedef enum {
 typedef enum { CC_SLIDING = 0, CC_FULL = 1 } cc_layer_type;
 typedef enum { CC_F32 = 0, CC_BF16 = 1 } cc_dtype;
 
+/* Which rotary index reads which position axis at which frequency (the half-dimension index
+ * k < head_dim/2, inv_freq[j] = theta^(-2j/head_dim)):
+ *  CC_MROPE_INTERLEAVED   mlxcel issue, "Text decoder forward", interleaved MRoPE: k reads
+ *                         axis h when k % 3 == 1 and k < 3 section[1], w when k % 3 == 2 and
+ *                         k < 3 section[2], else t, at frequency k.
+ *  CC_MROPE_SECTIONS_HWT  the same issue's acceptance notes (the RoPE correction): contiguous
+ *                         [H, W, T] sections with pre-permuted inv_freq. The permutation is
+ *                         not on the pages; read as: the H section (section[1] indices) takes,
+ *                         in increasing order, the frequencies the interleaved rule sends to h,
+ *                         then W (section[2]) those sent to w, then T the rest. */
+typedef enum { CC_MROPE_INTERLEAVED = 0, CC_MROPE_SECTIONS_HWT = 1 } cc_mrope_layout;
+
 /* Model hyper-parameters: the text_config keys of the Compass checkpoint (mlxcel issue,
  * "Config (config.json)" and "Text decoder forward"). `layer_types` points to
  * num_layers entries of cc_layer_type and is copied by cc_layer_plan_create.
@@ -77,6 +89,7 @@ typedef struct {
   double rope_theta;
   float layer_norm_eps;
   float logit_scale;
+  int32_t mrope_layout;       /* cc_mrope_layout (0: interleaved)                        */
 } cc_model_config;
 
 /* One layer's weights, packed by cc_pack_layer_weights:
@@ -352,6 +365,12 @@ cc_status cc_op_layernorm(const float* x, const void* gamma, void* out, int32_t 
 cc_status cc_op_mrope_table(const int32_t* pos, int32_t tokens, int32_t head_dim,
                             double theta, const int32_t* section_host, float* table,
                             void* stream);
+
+/* cc_op_mrope_table for a given cc_mrope_layout (the table of CC_MROPE_SECTIONS_HWT puts at
+ * rotary index k the axis and frequency of that layout). */
+cc_status cc_op_mrope_table_layout(const int32_t* pos, int32_t tokens, int32_t head_dim,
+                                   double theta, const int32_t* section_host, int32_t layout,
+                                   float* table, void* stream);
 
 /* The 4-bit affine GEMM of cc_decode_step_q4: C[M, N] = alpha * A[M, K] @ W^T (+ C when
  * accumulate != 0), W [N, K] in tiled form (cc_pack_q4_tiles), each weight rounded to bf16

@@ -100,6 +100,24 @@ def test_mrope_table_matches_oracle(section, theta):
     assert np.abs(got[..., 1] - sin[:, :d // 2]).max() < 2e-6
 
 
+@pytest.mark.parametrize("section,theta", [((24, 20, 20), 50000.0), ((12, 10, 10), 1e4),
+                                           ((16, 8, 8), 1e6)])
+def test_mrope_table_sections_layout_matches_oracle(section, theta):
+    """The contiguous [H, W, T]-section layout (parity unpinned: the oracle states a reading)."""
+    rng = np.random.default_rng(4)
+    T = 501
+    pos = rng.integers(0, 40000, size=(3, T)).astype(np.int32)
+    d = 2 * sum(section)
+    table = torch.empty(T, d // 2, 2, dtype=torch.float32, device="cuda")
+    L.cc_op_mrope_table_layout(torch.from_numpy(pos).cuda(), T, d, theta, section,
+                               "sections_hwt", table)
+    _sync()
+    cos, sin = O.mrope_cos_sin(pos, d, theta, section, "sections_hwt")
+    got = f64(table)
+    assert np.abs(got[..., 0] - cos[:, :d // 2]).max() < 2e-6
+    assert np.abs(got[..., 1] - sin[:, :d // 2]).max() < 2e-6
+
+
 # --------------------------------------------------------------------------- GEMM
 @pytest.mark.parametrize("m,n,k", [(128, 128, 64), (300, 384, 640), (64, 2560, 2048),
                                    (1, 1280, 128), (1000, 512, 1024)])

@@ -71,6 +71,21 @@ def test_small_stack_varlen_and_gqa_variants():
     _check(inp, gw, h, lg)
 
 
+def test_small_stack_sections_mrope_layout():
+    """Prefill and decode with the contiguous [H, W, T]-section MRoPE layout (parity unpinned:
+    the oracle states a reading of the permutation)."""
+    inp = _small("small_sec", [260], [ImageSpan(0, 20, 1, 6, 8)], 1,
+                 types=(SLIDING, FULL, SLIDING), mrope_layout="sections_hwt", seed=27)
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+    shape = small_shape(num_layers=2, layer_types=(SLIDING, FULL), window=70, heads=(8, 2),
+                        mrope_layout="sections_hwt")
+    dec = Inputs(Workload("dec_sec", shape, "decode", [], head_rows="all", seed=28,
+                          decode_batch=6, cache_len=120, page_size=16))
+    gw, h, lg = _run(dec)
+    _check(dec, gw, h, lg)
+
+
 def test_small_stack_mha_and_no_images():
     inp = _small("small3", [130], [], 0, types=(FULL, SLIDING), window=33, heads=(2, 2),
                  hidden=128, inter=128, vocab=256, seed=23)
