@@ -407,34 +407,88 @@ def attn_flops(inp):
 
 
 def prefill_e2e(gw, inp, K, W, dist, stream):
+    """The prefill through host buffers, as a serving loop runs it: every step copies its
+    inputs from pinned host memory and reads its logits back, inside the timed region. The
+    copies run on a second stream into two alternating input sets, so step i + 1's upload and
+    step i's read-back overlap step i's compute; the timed region ends when the last logits
+    are on the host."""
     import torch
     host_h = torch.from_numpy(inp.hidden).pin_memory()
     host_pos = gw.pos.cpu().pin_memory()
     host_cu = gw.cu.cpu().pin_memory()
-    host_rows = gw.ds_rows.cpu().pin_memory()
+    host_rows = gw.ds_rows.cpu().pin_memory() if gw.ds_rows is not None else None
     host_ds = [f.cpu().pin_memory() for f in gw.ds_feats]
-    n_out = len(inp.head_rows) * inp.shape.vocab_size
-    host_out = torch.empty(n_out, dtype=torch.float32).pin_memory()
-    dev_h = torch.empty_like(gw.hidden0)
-    logits = torch.empty(len(inp.head_rows), inp.shape.vocab_size, device="cuda")
-    bi = (host_h.numel() * 4 + host_pos.numel() * 4 + host_cu.numel() * 4 + host_rows.numel() * 4
+    n_rows = len(inp.head_rows)
+    n_out = n_rows * inp.shape.vocab_size
+    host_out = [torch.empty(n_out, dtype=torch.float32).pin_memory() for _ in range(2)]
+    sets = [dict(h=torch.empty_like(gw.hidden0), pos=torch.empty_like(gw.pos),
+                 cu=torch.empty_like(gw.cu),
+                 rows=torch.empty_like(gw.ds_rows) if gw.ds_rows is not None else None,
+                 ds=[torch.empty_like(f) for f in gw.ds_feats],
+                 logits=torch.empty(n_rows, inp.shape.vocab_size, device="cuda"))
+            for _ in range(2)]
+    copy = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # set b's inputs are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # the step that used set b has finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # set b's logits are on the host
+    bi = (host_h.numel() * 4 + host_pos.numel() * 4 + host_cu.numel() * 4
+          + (host_rows.numel() * 4 if host_rows is not None else 0)
           + sum(f.numel() * f.element_size() for f in host_ds))
     bo = n_out * 4
 
-    def step(i):
-        dev_h.copy_(host_h, non_blocking=True)
-        gw.pos.copy_(host_pos, non_blocking=True)
-        gw.cu.copy_(host_cu, non_blocking=True)
-        gw.ds_rows.copy_(host_rows, non_blocking=True)
-        for d, h in zip(gw.ds_feats, host_ds):
-            d.copy_(h, non_blocking=True)
-        gw.step(dev_h, logits)
-        host_out.copy_(logits.view(-1), non_blocking=True)
+    def upload(b):
+        st = sets[b]
+        with torch.cuda.stream(copy):
+            copy.wait_event(ev_done[b])
+            st["h"].copy_(host_h, non_blocking=True)
+            st["pos"].copy_(host_pos, non_blocking=True)
+            st["cu"].copy_(host_cu, non_blocking=True)
+            if host_rows is not None:
+                st["rows"].copy_(host_rows, non_blocking=True)
+            for d, h in zip(st["ds"], host_ds):
+                d.copy_(h, non_blocking=True)
+            ev_in[b].record(copy)
 
-    ms = time_steps(step, K, W, dist, stream)
+    def run(n, start_event=None):
+        if start_event is not None:
+            copy.wait_event(start_event)
+        upload(0)
+        for i in range(n):
+            b = i & 1
+            if i + 1 < n:
+                upload(1 - b)
+            st = sets[b]
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])             # the previous read-back of this set
+            gw.stack.prefill(st["h"], st["pos"], st["cu"], gw.n_seqs, st["rows"], st["ds"])
+            gw.logits(st["h"], st["logits"])
+            ev_done[b].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_done[b])
+                host_out[b].copy_(st["logits"].view(-1), non_blocking=True)
+                ev_out[b].record(copy)
+        stream.wait_event(ev_out[(n - 1) & 1])
+
+    for b in range(2):                              # all events recorded once
+        ev_done[b].record(stream)
+        ev_out[b].record(stream)
+    run(W)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    run(K, t0)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    ms = dist.max(t0.elapsed_time(t1))
     T = inp.wl.total_tokens
     return {"value": T * K * dist.world / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms / K,
-            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+            "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+            "overlap": "uploads and read-backs on a second stream, two alternating input sets"}
 
 
 def decode_leg(args, dist, pk):
