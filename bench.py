@@ -35,10 +35,11 @@ PREFILL_DESC = ("two-layer pair (sliding+interleaved MRoPE, full NoPE), bf16, ba
                 "seq 2048, hidden 2048, 16/4 heads, head_dim 128, SwiGLU 8192, window 512, "
                 "one 16x16 image at token 300, deepstack [256,2048] after layer 0, tied head "
                 "on the last token, vocab 256000")
+PREFILL_WORKLOADS = {"pair": "pair_T2048", "stack28": "stack28_T8192", "varlen": "varlen_T32768"}
 PREFILL_OTHER = {
-    3: ("28-layer stack (full attention at every 4th layer), bf16, batch 1, seq 8192, window "
+    "stack28": ("28-layer stack (full attention at every 4th layer), bf16, batch 1, seq 8192, window "
         "4096, three 32x32 images, deepstack after layers 0-2, tied head on the last token"),
-    5: ("two-layer pair, varlen packed prefill of 4096/8192/12288/8192 tokens (T = 32768), "
+    "varlen": ("two-layer pair, varlen packed prefill of 4096/8192/12288/8192 tokens (T = 32768), "
         "window 4096, 1-4 images per sequence, deepstack after layers 0-1, head on the last "
         "token of each sequence"),
 }
@@ -59,9 +60,9 @@ def parse():
     p.add_argument("--no-q4", action="store_true", help="skip the 4-bit weight decode timing")
     p.add_argument("--cpu-tokens", type=int, default=0,
                    help="oracle sample: first N tokens of the prefill workload (0: all)")
-    p.add_argument("--prefill-config", type=int, choices=[2, 3, 5], default=2,
-                   help="prefill workload: 2 = two-layer pair T=2048 (the headline), "
-                        "3 = 28-layer stack T=8192, 5 = varlen packed T=32768")
+    p.add_argument("--prefill-workload", choices=["pair", "stack28", "varlen"], default="pair",
+                   help="prefill workload: pair = two-layer pair T=2048 (the headline), "
+                        "stack28 = 28-layer stack T=8192, varlen = varlen packed T=32768")
     return p.parse_args()
 
 
@@ -226,11 +227,11 @@ def prefill_leg(args, dist, pk):
     import numpy as np
     import torch
     from synth import Inputs
-    from synth.configs import cfg2
+    from synth.configs import pair_T2048
     from cohere_compass_decoder_gb300.workload import GpuWorkload
 
-    from synth.configs import CONFIGS
-    inp = Inputs(CONFIGS[args.prefill_config]())
+    from synth.configs import WORKLOADS
+    inp = Inputs(WORKLOADS[PREFILL_WORKLOADS[args.prefill_workload]]())
     gw = GpuWorkload(inp)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -252,7 +253,7 @@ def prefill_leg(args, dist, pk):
     ach = flops / (g1["avg_us"] * 1e-6) / 1e12 if g1 else None
     roof = {"kernel": "gemm_qkv_mlp", "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
             "unit": "TFLOP/s", "frac": (ach / pk["bf16"]) if ach else None,
-            "traffic": measured_traffic("gemm_qkv_mlp") if args.prefill_config == 2 else None,
+            "traffic": measured_traffic("gemm_qkv_mlp") if args.prefill_workload == "pair" else None,
             "peak_source": f"{pk['src']} bf16 burst (of {pk['src']})",
             "algorithmic_per_launch": f"2*T*N1*H = {flops:.4g} FLOP"}
     # other classes against their own roofs
@@ -275,7 +276,7 @@ def prefill_leg(args, dist, pk):
                batch=len(inp.wl.seq_lens))
     if s.dtype == "bf16":
         res["next_rows"] = {"embed_merge_ln": embed_merge_timing(inp, gw, pk)}
-        if args.prefill_config == 2:
+        if args.prefill_workload == "pair":
             res["next_rows"]["chunked_prefill"] = chunked_prefill_timing(inp, gw, pk)
     # e2e through host buffers
     if not args.no_e2e:
@@ -494,10 +495,10 @@ def prefill_e2e(gw, inp, K, W, dist, stream):
 def decode_leg(args, dist, pk):
     import torch
     from synth import Inputs
-    from synth.configs import cfg4
+    from synth.configs import decode_B64_cache4096
     from cohere_compass_decoder_gb300.workload import GpuWorkload
 
-    inp = Inputs(cfg4())
+    inp = Inputs(decode_B64_cache4096())
     gw = GpuWorkload(inp)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -602,10 +603,10 @@ def cpu_baseline(args, tokens=0):
     """The oracle (fp64 NumPy, as it stands) on the prefill workload or its first tokens."""
     import numpy as np
     from synth import Inputs
-    from synth.configs import cfg2, Workload
+    from synth.configs import pair_T2048, Workload
     from oracle import runs
 
-    wl = cfg2()
+    wl = pair_T2048()
     if tokens and tokens < wl.total_tokens:
         imgs = [i for i in wl.images if i.start + i.n_tokens <= tokens]
         wl = Workload(wl.name + f"_first{tokens}", wl.shape, "prefill", [tokens], images=imgs,
@@ -682,8 +683,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": PREFILL_DESC if args.prefill_config == 2 else
-                       PREFILL_OTHER[args.prefill_config],
+            "config": {"workload": PREFILL_DESC if args.prefill_workload == "pair" else
+                       PREFILL_OTHER[args.prefill_workload],
                        "global_batch": pre["batch"], "seq_len": pre["tokens"],
                        "parallelism": "replicas" if dist.world > 1 else "single",
                        "l2": "inputs larger than L2 (1.3 GB of weights per step)"},

@@ -83,47 +83,47 @@ def _pattern_3to1(n):
     return tuple(FULL if i % 4 == 3 else SLIDING for i in range(n))
 
 
-SHAPE_CFG1 = ModelShape(
+SHAPE_LAYER_FP32 = ModelShape(
     num_layers=1, hidden_size=256, num_attention_heads=4, num_key_value_heads=1,
     head_dim=64, intermediate_size=512, vocab_size=1024, sliding_window=32,
     mrope_section=(12, 10, 10), rope_theta=1e4, layer_types=(SLIDING,),
     layer_norm_eps=1e-5, logit_scale=0.0625, dtype="f32")
 
-# config-2 per-layer shapes (also used by the 28-layer stack, the decode step and
-# the varlen prefill); rope theta 50000 as in the real model.
+# the two-layer pair's per-layer shapes (also used by the 28-layer stack, the decode step
+# and the varlen prefill); rope theta 50000 as in the real model.
 _C2 = dict(hidden_size=2048, num_attention_heads=16, num_key_value_heads=4, head_dim=128,
            intermediate_size=8192, vocab_size=256000, mrope_section=(24, 20, 20),
            rope_theta=50000.0, layer_norm_eps=1e-5, logit_scale=0.0625, dtype="bf16")
 
-SHAPE_CFG2 = ModelShape(num_layers=2, sliding_window=512, layer_types=(SLIDING, FULL), **_C2)
-SHAPE_CFG3 = ModelShape(num_layers=28, sliding_window=4096, layer_types=_pattern_3to1(28), **_C2)
-SHAPE_CFG45 = ModelShape(num_layers=2, sliding_window=4096, layer_types=(SLIDING, FULL), **_C2)
+SHAPE_PAIR = ModelShape(num_layers=2, sliding_window=512, layer_types=(SLIDING, FULL), **_C2)
+SHAPE_STACK28 = ModelShape(num_layers=28, sliding_window=4096, layer_types=_pattern_3to1(28), **_C2)
+SHAPE_PAIR_W4096 = ModelShape(num_layers=2, sliding_window=4096, layer_types=(SLIDING, FULL), **_C2)
 
 
-def cfg1() -> Workload:
-    return Workload("cfg1_layer_fp32_T128", SHAPE_CFG1, "prefill", [128],
+def layer_fp32_T128() -> Workload:
+    return Workload("layer_fp32_T128", SHAPE_LAYER_FP32, "prefill", [128],
                     images=[ImageSpan(0, 48, 1, 4, 4)], n_deepstack=1, head_rows="all", seed=1)
 
 
-def cfg2() -> Workload:
-    return Workload("cfg2_pair_bf16_T2048", SHAPE_CFG2, "prefill", [2048],
+def pair_T2048() -> Workload:
+    return Workload("pair_bf16_T2048", SHAPE_PAIR, "prefill", [2048],
                     images=[ImageSpan(0, 300, 1, 16, 16)], n_deepstack=1, head_rows="last", seed=2)
 
 
-def cfg3() -> Workload:
+def stack28_T8192() -> Workload:
     # three 32x32 images interleaved with text at fixed offsets
     imgs = [ImageSpan(0, s, 1, 32, 32) for s in (1280, 3584, 5888)]
-    return Workload("cfg3_stack28_bf16_T8192", SHAPE_CFG3, "prefill", [8192],
+    return Workload("stack28_bf16_T8192", SHAPE_STACK28, "prefill", [8192],
                     images=imgs, n_deepstack=3, head_rows="last", seed=3)
 
 
-def cfg4() -> Workload:
-    return Workload("cfg4_decode_B64_cache4096", SHAPE_CFG45, "decode", [],
+def decode_B64_cache4096() -> Workload:
+    return Workload("decode_B64_cache4096", SHAPE_PAIR_W4096, "decode", [],
                     n_deepstack=0, head_rows="all", seed=4,
                     decode_batch=64, cache_len=4096, page_size=16)
 
 
-def cfg5_images(seq_lens, seed=5) -> List[ImageSpan]:
+def varlen_images(seq_lens, seed=5) -> List[ImageSpan]:
     """Seeded image layout of the varlen workload: per sequence 1-4 square merged grids
     of side 24..48, separated by text gaps of at least 64 tokens."""
     import numpy as np
@@ -148,14 +148,16 @@ def cfg5_images(seq_lens, seed=5) -> List[ImageSpan]:
     return out
 
 
-def cfg5() -> Workload:
+def varlen_T32768() -> Workload:
     lens = [4096, 8192, 12288, 8192]
     # The 2-layer stack has no layer 2, so deepstack goes after layers 0 and 1 only.
-    return Workload("cfg5_varlen_bf16_T32768", SHAPE_CFG45, "prefill", lens,
-                    images=cfg5_images(lens), n_deepstack=2, head_rows="last", seed=5)
+    return Workload("varlen_bf16_T32768", SHAPE_PAIR_W4096, "prefill", lens,
+                    images=varlen_images(lens), n_deepstack=2, head_rows="last", seed=5)
 
 
-CONFIGS = {1: cfg1, 2: cfg2, 3: cfg3, 4: cfg4, 5: cfg5}
+WORKLOADS = {"layer_fp32_T128": layer_fp32_T128, "pair_T2048": pair_T2048,
+             "stack28_T8192": stack28_T8192, "decode_B64_cache4096": decode_B64_cache4096,
+             "varlen_T32768": varlen_T32768}
 
 
 def small_shape(num_layers=2, layer_types=None, window=64, dtype="bf16", hidden=256,

@@ -9,7 +9,7 @@ import pytest
 
 from conftest import ROOT
 from oracle import decoder as O
-from synth.configs import cfg1, cfg2, cfg3, cfg5, ImageSpan
+from synth.configs import layer_fp32_T128, pair_T2048, stack28_T8192, varlen_T32768, ImageSpan
 
 import cohere_compass_decoder_gb300._lib as L
 
@@ -45,7 +45,7 @@ def _spans(wl):
     return [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w) for i in wl.images]
 
 
-@pytest.mark.parametrize("make", [cfg1, cfg2, cfg3, cfg5])
+@pytest.mark.parametrize("make", [layer_fp32_T128, pair_T2048, stack28_T8192, varlen_T32768])
 def test_positions_bit_exact_on_workloads(lib, make):
     wl = make()
     pos, delta = L.cc_build_mrope_positions(_spans(wl), wl.seq_lens)

@@ -12,7 +12,7 @@ import torch
 
 from oracle import runs as R
 from synth import Inputs, Workload, ImageSpan, small_shape, SLIDING, FULL
-from synth.configs import cfg1, cfg2, cfg3, cfg4, cfg5
+from synth.configs import layer_fp32_T128, pair_T2048, stack28_T8192, decode_B64_cache4096, varlen_T32768
 from cohere_compass_decoder_gb300.workload import GpuWorkload, as_numpy
 from cohere_compass_decoder_gb300.model import to_device
 import cohere_compass_decoder_gb300._lib as L
@@ -86,6 +86,17 @@ def test_small_stack_sections_mrope_layout():
     _check(dec, gw, h, lg)
 
 
+def test_small_stack_with_empty_sequences():
+    """Empty sequences inside a packed batch (equal cu_seqlens entries) contribute no tokens,
+    no positions and no work; the others are unaffected (reading: an empty sequence has no
+    positions and rope_delta 0)."""
+    inp = _small("small_empty", [0, 150, 0, 0, 91, 0], [ImageSpan(1, 30, 1, 4, 5),
+                                                          ImageSpan(4, 0, 1, 3, 3)], 2,
+                 types=(SLIDING, FULL), window=70, seed=29)
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
 def test_small_stack_mha_and_no_images():
     inp = _small("small3", [130], [], 0, types=(FULL, SLIDING), window=33, heads=(2, 2),
                  hidden=128, inter=128, vocab=256, seed=23)
@@ -137,14 +148,14 @@ def test_causal_prefix_on_gpu():
 
 
 # ------------------------------------------------------------------------- the five workloads
-def test_cfg1_single_layer_fp32():
-    inp = Inputs(cfg1())
+def test_single_layer_fp32_T128():
+    inp = Inputs(layer_fp32_T128())
     gw, h, lg = _run(inp)
     _check(inp, gw, h, lg, tol=(1e-4, 1e-5), lg_rel=1e-4)
 
 
-def test_cfg2_two_layer_pair():
-    inp = Inputs(cfg2())
+def test_two_layer_pair_T2048():
+    inp = Inputs(pair_T2048())
     gw, h, lg = _run(inp)
     _check(inp, gw, h, lg)
 
@@ -182,8 +193,8 @@ def test_small_decode_step_q4():
     assert np.abs(as_numpy(h) - R.run_decode(inp)[0]).max() > 1e-2
 
 
-def test_cfg4_decode_step():
-    inp = Inputs(cfg4())
+def test_decode_step_B64_cache4096():
+    inp = Inputs(decode_B64_cache4096())
     gw, h, lg = _run(inp)
     _check(inp, gw, h, lg)
 
@@ -278,10 +289,10 @@ def test_chunked_prefill_over_a_paged_prefix():
 
 
 @pytest.fixture(scope="module")
-def cfg3_oracle():
+def stack28_oracle():
     """The 28-layer workload's inputs and the oracle's residual stream after every layer."""
     from oracle import decoder as O
-    inp = Inputs(cfg3())
+    inp = Inputs(stack28_T8192())
     wl = inp.wl
     pos, _ = O.positions(wl.seq_lens, [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w)
                                        for i in wl.images])
@@ -313,11 +324,11 @@ class _OneLayer(Inputs):
 
 
 @pytest.mark.slow
-def test_cfg3_every_layer_from_oracle_input(cfg3_oracle):
+def test_stack28_every_layer_from_oracle_input(stack28_oracle):
     """Each of the 28 layers (with its deepstack add) on the GPU, started from the oracle's
     residual stream before it, matches the oracle's stream after it within the stack
     tolerance (2e-2 max-abs, 2e-3 mean-abs)."""
-    inp, hs, _ = cfg3_oracle
+    inp, hs, _ = stack28_oracle
     prev = inp.hidden.astype(np.float64)
     worst = []
     for i in range(inp.shape.num_layers):
@@ -334,14 +345,14 @@ def test_cfg3_every_layer_from_oracle_input(cfg3_oracle):
 
 
 @pytest.mark.slow
-def test_cfg3_stack28(cfg3_oracle):
+def test_stack28_T8192(stack28_oracle):
     """The whole 28-layer stack and the head, end to end. Two bf16 implementations that
     round the same intermediates drift apart by independent rounding noise once any
     residual differs by an ulp; the oracle's own bf16-mirror mode drifts from its exact fp64
     mode by 0.040 mean-abs / 0.24 max-abs after these 28 layers (per-layer growth about
     1.4e-3). The end-to-end bound is therefore 1.5x that floor: 0.06 mean-abs, 0.5 max-abs
     on the final hidden state; the logits keep the stack tolerance."""
-    inp, hs, lg_ref = cfg3_oracle
+    inp, hs, lg_ref = stack28_oracle
     gw, h, lg = _run(inp)
     assert_close(as_numpy(h), hs[-1], 0.5, 0.06, "hidden after 28 layers")
     lmx, _ = assert_close(as_numpy(lg), lg_ref, TOL_MAX, TOL_MEAN, "logits")
@@ -349,7 +360,7 @@ def test_cfg3_stack28(cfg3_oracle):
 
 
 @pytest.mark.slow
-def test_cfg5_varlen():
-    inp = Inputs(cfg5())
+def test_varlen_T32768():
+    inp = Inputs(varlen_T32768())
     gw, h, lg = _run(inp)
     _check(inp, gw, h, lg)

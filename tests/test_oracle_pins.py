@@ -16,7 +16,7 @@ import torch
 import oracle
 from oracle import decoder as O
 from synth import Inputs, Workload, ImageSpan, small_shape, SLIDING, FULL
-from synth.configs import SHAPE_CFG3, cfg1, cfg5
+from synth.configs import SHAPE_STACK28, layer_fp32_T128, varlen_T32768
 
 from conftest import read_golden
 
@@ -159,7 +159,7 @@ def test_rope_preserves_pair_norms():
 
 # ----------------------------------------------------------------------------- positions
 def test_positions_closed_form_single_layer_workload():
-    wl = cfg1()
+    wl = layer_fp32_T128()
     pos, delta = O.positions(wl.seq_lens, [(i.seq, i.start, i.grid_t, i.grid_h, i.grid_w)
                                            for i in wl.images])
     want = np.zeros((3, 128), dtype=np.int64)
@@ -195,12 +195,12 @@ def test_decode_positions_add_rope_delta():
 
 def test_layer_pattern_matches_page():
     g = read_golden("layer_pattern_28.txt")
-    full = [i for i, t in enumerate(SHAPE_CFG3.layer_types) if t == FULL]
+    full = [i for i, t in enumerate(SHAPE_STACK28.layer_types) if t == FULL]
     assert full == g["full"]
 
 
 def test_varlen_layout_is_valid():
-    wl = cfg5()
+    wl = varlen_T32768()
     for s, L in enumerate(wl.seq_lens):
         ims = sorted([i for i in wl.images if i.seq == s], key=lambda i: i.start)
         assert 1 <= len(ims) <= 4
