@@ -54,20 +54,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the phase of parity `parity`; its result can be consumed well after
-// it is issued, so a thread can overlap the test with other work.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Waits until the phase of parity `parity` of the barrier has completed. Gives up, sets
 // *err = CC_DEV_TIMEOUT and returns false after about kWaitTimeoutCycles SM clocks, or
 // returns false early when *err is already set (another warp or an earlier launch gave
@@ -219,6 +205,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 
 #define CC_R32(i) CC_R8(i), CC_R8(i + 8), CC_R8(i + 16), CC_R8(i + 24)
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane, waiting for the load.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : CC_R8(0), CC_R8(8)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 // 64 consecutive 32-bit TMEM columns of this thread's lane, waiting for the load.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
