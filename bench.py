@@ -536,10 +536,53 @@ def decode_leg(args, dist, pk):
     launches = sum(v["launches_per_step"] for v in kern.values())
     launches += kern.get("attn_decode", {}).get("launches_per_step", 0)  # + split combine
     res = dict(ms=ms, value=value, kernels=kern, roofline=roof, launches=int(round(launches * K)))
+    res["next_rows"] = {"decode_graph": decode_graph_timing(gw, inp, steps=max(K, 10))}
     if not args.no_q4:
-        res["next_rows"] = {"decode_q4": decode_q4_timing(inp, gw, pk)}
+        res["next_rows"]["decode_q4"] = decode_q4_timing(inp, gw, pk)
     gw.close()
     return res
+
+
+def decode_graph_timing(gw, inp, steps=20):
+    """The decode step + head captured once into a CUDA graph (the hidden-state reset
+    included) and replayed, against the same work launched eagerly: what a serving loop that
+    replays one graph per step saves in launch overhead."""
+    import torch
+    n = int(gw.head_rows.numel())
+    h = gw.fresh_hidden()
+    lg = torch.empty(n, inp.shape.vocab_size, dtype=torch.float32, device="cuda")
+
+    def once():
+        h.copy_(gw.hidden0)
+        gw.step(h, lg)
+    once()                                   # sizes the plan's scratch before capture
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        once()
+    torch.cuda.current_stream().wait_stream(side)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+    eager = timed(once)
+    graph = timed(g.replay)
+    gw.sync()
+    B = inp.wl.decode_batch
+    return {"ms_per_step_graph": graph, "ms_per_step_eager": eager,
+            "tokens_per_s_graph": B / (graph / 1e3),
+            "note": "cc_decode_step + cc_logits (and the hidden-state reset) captured in one CUDA "
+                    "graph and replayed, against the same calls launched eagerly"}
 
 
 def decode_q4_timing(inp, gw, pk, steps=10):

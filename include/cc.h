@@ -301,6 +301,13 @@ cc_status cc_decode_step_q4(cc_layer_plan* plan, float* hidden, const int32_t* p
 cc_status cc_logits_q4(cc_layer_plan* plan, const float* hidden, const int32_t* rows,
                        int32_t n_rows, float* logits, void* stream);
 
+/* CUDA graphs: cc_prefill_forward, cc_prefill_forward_tokens, cc_prefill_forward_chunk,
+ * cc_decode_step(_q4) and cc_logits(_q4) enqueue kernels (and, for a split head, one memset)
+ * on `stream` only: no allocation and no host synchronisation, except that cc_decode_step
+ * grows the plan's split-KV scratch (cudaMalloc after a stream synchronize) the first time a
+ * call needs more. After one eager call of the same shape they can be captured into a CUDA
+ * graph by stream capture and replayed; the arguments (device pointers, sizes) are baked in. */
+
 /* Waits for `stream`, then returns and clears the plan's sticky device error flag
  * (CC_ERR_TIMEOUT / CC_ERR_DEVICE_CHECK), or CC_ERR_CUDA if the stream failed. */
 cc_status cc_sync(cc_layer_plan* plan, void* stream);

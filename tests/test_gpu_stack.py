@@ -193,6 +193,68 @@ def test_small_decode_step_q4():
     assert np.abs(as_numpy(h) - R.run_decode(inp)[0]).max() > 1e-2
 
 
+def _graph_replay(gw, step):
+    """step(hidden, logits) captured into a CUDA graph after one eager call (which sizes the
+    plan's scratch), replayed on a fresh hidden state; returns (eager h, eager logits, replayed
+    h, replayed logits)."""
+    h_e = gw.fresh_hidden()
+    lg_e = step(h_e, None)
+    gw.sync()
+    h = gw.fresh_hidden()
+    lg = torch.empty_like(lg_e)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        step(h, lg)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):                       # replays start from the same input each time
+        h.copy_(gw.hidden0)
+        g.replay()
+    torch.cuda.synchronize()
+    gw.sync()
+    return h_e, lg_e, h, lg
+
+
+def test_decode_step_replays_from_a_cuda_graph():
+    """The decode step and the head make no allocation and no host synchronisation once the
+    plan's scratch fits the call: captured into a CUDA graph, a replay gives the eager results
+    (up to the order of the split-K atomic adds into h)."""
+    inp = _small_decode(seed=41, B=5)
+    gw = GpuWorkload(inp)
+    h_e, lg_e, h, lg = _graph_replay(gw, lambda hid, out: gw.step(hid, out))
+    assert_close(as_numpy(h), as_numpy(h_e), 1e-4, 1e-6, "hidden (graph vs eager)")
+    assert_close(as_numpy(lg), as_numpy(lg_e), 1e-4, 1e-6, "logits (graph vs eager)")
+    gw.close()
+
+
+def test_decode_step_q4_replays_from_a_cuda_graph():
+    inp = _small_decode(seed=43, B=6)
+    gw = GpuWorkload(inp)
+    gw.stack.attach_q4(inp.layer_q4, inp.embed_q4)
+    n = int(gw.head_rows.numel())
+
+    def step(hid, out):
+        if out is None:
+            out = torch.empty(n, inp.shape.vocab_size, dtype=torch.float32, device="cuda")
+        gw.stack.decode_q4(hid, gw.pos, gw.seq_lens, gw.page_table, gw.max_pages, gw.kv)
+        gw.stack.logits_q4(hid, gw.head_rows, n, out)
+        return out
+    h_e, lg_e, h, lg = _graph_replay(gw, step)
+    assert_close(as_numpy(h), as_numpy(h_e), 1e-4, 1e-6, "hidden (q4 graph vs eager)")
+    assert_close(as_numpy(lg), as_numpy(lg_e), 1e-4, 1e-6, "logits (q4 graph vs eager)")
+    gw.close()
+
+
+def test_prefill_replays_from_a_cuda_graph():
+    inp = _small("small_graph", [200, 77], [ImageSpan(0, 40, 1, 4, 6)], 2, seed=45)
+    gw = GpuWorkload(inp)
+    h_e, lg_e, h, lg = _graph_replay(gw, lambda hid, out: gw.step(hid, out))
+    assert_close(as_numpy(h), as_numpy(h_e), 1e-4, 1e-6, "hidden (prefill graph vs eager)")
+    assert_close(as_numpy(lg), as_numpy(lg_e), 1e-4, 1e-6, "logits (prefill graph vs eager)")
+    gw.close()
+
+
 def test_decode_step_B64_cache4096():
     inp = Inputs(decode_B64_cache4096())
     gw, h, lg = _run(inp)
