@@ -125,3 +125,40 @@ def test_struct_layouts_match_header(tmp_path):
         assert int(out[name]) == C.sizeof(st), name
         for fname, _ in st._fields_:
             assert int(out[f"{name}.{fname}"]) == getattr(st, fname).offset, (name, fname)
+
+
+# ------------------------------------------------------------ host-side checks of the next rows
+def test_q4_tiled_bytes(lib):
+    """Blocks of 128 rows x 128 K, 9216 bytes each; an odd number of 64-K groups rounds up."""
+    assert lib.cc_q4_tiled_bytes(128, 128) == 9216
+    assert lib.cc_q4_tiled_bytes(256, 2048) == 2 * 16 * 9216
+    assert lib.cc_q4_tiled_bytes(19456, 2048) == 152 * 16 * 9216
+    assert lib.cc_q4_tiled_bytes(2048, 10240) == 16 * 80 * 9216
+    assert lib.cc_q4_tiled_bytes(128, 192) == 2 * 9216          # 3 groups -> 2 blocks
+    for rows, k in [(100, 128), (128, 100), (0, 64), (128, 0), (-128, 64)]:
+        assert lib.cc_q4_tiled_bytes(rows, k) == 0
+
+
+def test_q4_entry_points_reject_bad_arguments_before_any_device_work(lib):
+    dummy = 256      # never dereferenced: the checks come first
+    assert lib.cc_pack_q4_tiles(dummy, dummy, dummy, 100, 128, dummy, None) == L.CC_ERR_UNSUPPORTED
+    assert lib.cc_pack_q4_tiles(dummy, dummy, dummy, 128, 96, dummy, None) == L.CC_ERR_UNSUPPORTED
+    assert lib.cc_pack_q4_tiles(None, dummy, dummy, 128, 128, dummy, None) == L.CC_ERR_INVALID_ARG
+    assert lib.cc_pack_q4_tiles(dummy, dummy, dummy, 0, 128, dummy, None) == L.CC_OK
+    assert lib.cc_op_gemm_q4(dummy, dummy, dummy, 129, 128, 64, 1.0, 0, None) == L.CC_ERR_UNSUPPORTED
+    assert lib.cc_op_gemm_q4(dummy, dummy, dummy, 64, 100, 64, 1.0, 0, None) == L.CC_ERR_UNSUPPORTED
+    assert lib.cc_op_gemm_q4(None, dummy, dummy, 64, 128, 64, 1.0, 0, None) == L.CC_ERR_INVALID_ARG
+    assert lib.cc_op_gemm_q4(dummy, dummy, dummy, 0, 128, 64, 1.0, 0, None) == L.CC_OK
+    assert lib.cc_layer_plan_attach_q4(None, None, None) == L.CC_ERR_INVALID_ARG
+    assert lib.cc_decode_step_q4(None, None, None, None, None, 0, 0, None, None) == L.CC_ERR_INVALID_ARG
+    assert lib.cc_logits_q4(None, None, None, 0, None, None) == L.CC_ERR_INVALID_ARG
+
+
+def test_mrope_layout_argument_is_checked(lib):
+    section = L._i32_array((24, 20, 20))
+    for layout in (2, -1):
+        assert lib.cc_op_mrope_table_layout(256, 4, 128, 5e4, section, layout, 256, None) == \
+            L.CC_ERR_INVALID_ARG
+    bad = L._i32_array((24, 20, 21))   # does not sum to head_dim / 2
+    assert lib.cc_op_mrope_table_layout(256, 4, 128, 5e4, bad, 1, 256, None) == L.CC_ERR_INVALID_ARG
+    assert lib.cc_op_mrope_table_layout(256, 0, 128, 5e4, section, 1, 256, None) == L.CC_OK
