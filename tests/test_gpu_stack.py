@@ -261,6 +261,25 @@ def test_decode_step_B64_cache4096():
     _check(inp, gw, h, lg)
 
 
+def test_decode_step_q4_B64_cache4096():
+    """The 4-bit decode step and head at the size the bench times (64 sequences x 4096 cached
+    tokens, the two-layer pair, vocab 256000) against the oracle on the dequantised weights."""
+    inp = Inputs(decode_B64_cache4096())
+    gw = GpuWorkload(inp)
+    gw.stack.attach_q4(inp.layer_q4, inp.embed_q4)
+    h = gw.fresh_hidden()
+    n = int(gw.head_rows.numel())
+    lg = torch.empty(n, inp.shape.vocab_size, dtype=torch.float32, device="cuda")
+    gw.stack.decode_q4(h, gw.pos, gw.seq_lens, gw.page_table, gw.max_pages, gw.kv)
+    gw.stack.logits_q4(h, gw.head_rows, n, lg)
+    gw.sync()
+    h_ref, lg_ref = R.run_decode_q4(inp)
+    assert_close(as_numpy(h), h_ref, TOL_MAX, TOL_MEAN, "hidden")
+    lmx, _ = assert_close(as_numpy(lg), lg_ref, TOL_MAX, TOL_MEAN, "logits")
+    assert lmx / np.abs(lg_ref).max() <= 2e-2
+    gw.close()
+
+
 def test_decode_continues_prefill_on_gpu():
     """Prefill of L tokens fills the paged cache; decoding token L+1 then matches the last
     row of an (L+1)-token prefill (both on the GPU)."""
