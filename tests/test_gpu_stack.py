@@ -369,6 +369,73 @@ def test_chunked_prefill_over_a_paged_prefix():
         assert_close(as_numpy(got), h_ref[rows], TOL_MAX, TOL_MEAN, "chunk vs oracle")
 
 
+def test_prefill_from_token_ids_pair_T2048():
+    """The token-id prefill (embedding merge fused with layer 0's LayerNorm) at the size the
+    bench times: the two-layer pair, 2048 tokens, one 16x16 image, vocab 256000."""
+    from oracle import decoder as OD
+    inp = Inputs(pair_T2048())
+    gw = GpuWorkload(inp)
+    s = inp.shape
+    T = inp.wl.total_tokens
+    tok = torch.from_numpy(inp.token_ids).cuda()
+    rows = torch.from_numpy(inp.mm_rows.astype(np.int32)).cuda()
+    feats = to_device(inp.mm_embeds)
+    h = torch.empty(T, s.hidden_size, dtype=torch.float32, device="cuda")
+    gw.stack.prefill_tokens(tok, rows, feats, h, gw.pos, gw.cu, gw.n_seqs, gw.ds_rows, gw.ds_feats)
+    gw.sync()
+    h0 = OD.embed_merge(inp.token_ids, OD.from_storage(inp.embed), inp.mm_rows,
+                        OD.from_storage(inp.mm_embeds))
+    h_ref, _ = R.run_prefill(inp, hidden=h0)
+    assert_close(as_numpy(h), h_ref, TOL_MAX, TOL_MEAN, "hidden")
+    gw.close()
+
+
+def test_chunked_prefill_pair_2048_after_2048():
+    """The chunked prefill at the size the bench times: a 4096-token sequence of the two-layer
+    pair, the first 2048 tokens prefilled into the paged cache, the next 2048 continuing them
+    (an image span crosses the boundary); both chunks equal the rows of the oracle's whole
+    prefill."""
+    from synth.configs import SHAPE_PAIR
+    T, cut = 4096, 2048
+    inp = Inputs(Workload("pair_T4096_chunked", SHAPE_PAIR, "prefill", [T],
+                          images=[ImageSpan(0, 300, 1, 16, 16), ImageSpan(0, 1900, 1, 16, 16)],
+                          n_deepstack=1, head_rows="last", seed=47))
+    h_ref, _ = R.run_prefill(inp)
+    gw = GpuWorkload(inp, max_tokens=cut)
+    st = gw.stack
+    s = inp.shape
+    ps, max_pages = 16, T // 16
+    table = torch.tensor(np.random.default_rng(3).permutation(max_pages + 5)[:max_pages]
+                         .reshape(1, max_pages), dtype=torch.int32, device="cuda")
+    kp = [torch.zeros(max_pages + 5, s.num_key_value_heads, ps, 128, dtype=torch.bfloat16,
+                      device="cuda") for _ in range(s.num_layers)]
+    vp = [torch.zeros_like(t) for t in kp]
+    kv = L.make_kv_pool(kp, vp, max_pages + 5)
+    pos_full = gw.pos.cpu().numpy()
+    ds_rows = inp.ds_rows
+
+    def chunk(lo, hi):
+        h = torch.from_numpy(inp.hidden[lo:hi].copy()).cuda()
+        pos = torch.from_numpy(np.ascontiguousarray(pos_full[:, lo:hi])).cuda()
+        cu = torch.tensor([0, hi - lo], dtype=torch.int32, device="cuda")
+        sel = [k for k, r in enumerate(ds_rows) if lo <= int(r) < hi]
+        dr = torch.tensor([int(ds_rows[k]) - lo for k in sel], dtype=torch.int32, device="cuda")
+        ds = [to_device(inp.ds(0)[sel])]
+        return h, pos, cu, dr, ds
+
+    h1, pos1, cu1, dr1, ds1 = chunk(0, cut)
+    L.cc_prefill_forward(st.plan, h1, pos1, cu1, 1, cut, dr1, int(dr1.numel()), ds1, kv, table,
+                         max_pages)
+    h2, pos2, cu2, dr2, ds2 = chunk(cut, T)
+    prefix = torch.tensor([cut], dtype=torch.int32, device="cuda")
+    L.cc_prefill_forward_chunk(st.plan, h2, pos2, cu2, 1, T - cut, prefix, kv, table, max_pages,
+                               dr2, int(dr2.numel()), ds2)
+    st.sync()
+    assert_close(as_numpy(h1), h_ref[:cut], TOL_MAX, TOL_MEAN, "first chunk vs oracle")
+    assert_close(as_numpy(h2), h_ref[cut:], TOL_MAX, TOL_MEAN, "second chunk vs oracle")
+    gw.close()
+
+
 @pytest.fixture(scope="module")
 def stack28_oracle():
     """The 28-layer workload's inputs and the oracle's residual stream after every layer."""
