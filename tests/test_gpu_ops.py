@@ -325,6 +325,95 @@ def test_attention_window_at_least_sequence_equals_full():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
+
+# --------------------------------------------------------------------------- mask membership
+# With zero queries every score is 0, so every visible key gets weight exactly 1 and P V
+# sums exact integers. With V[j] = e_(j mod 128) (one-hot by key position), output column c
+# of a query is (its visible keys j with j = c mod 128) / (its visible keys): a closed form
+# of the visible set. One key too many or too few moves that key's column by at least a
+# third, far outside one bf16 rounding, so this checks the causal / window / sequence masks
+# key by key (the random-input parity tests bound such an error only through the tolerance).
+def _onehot_by_position(n, nkv):
+    v = np.zeros((n, nkv, 128))
+    v[np.arange(n), :, np.arange(n) % 128] = 1.0
+    return v
+
+
+def _visible_fraction(lo, hi):
+    """Column c: #{lo <= j <= hi : j = c mod 128} / (hi - lo + 1)."""
+    c = np.arange(128)
+    first = lo + (c - lo) % 128
+    cnt = np.where(first <= hi, (hi - first) // 128 + 1, 0)
+    return cnt / (hi - lo + 1)
+
+
+def _assert_one_rounding(got, want, what):
+    # bf16(count * fp32(1/n)): within one bf16 rounding (2^-8 relative); absent keys give 0
+    bad = np.abs(got - want) > want * 2.0 ** -8 * 1.01
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off, first at {np.argwhere(bad)[0]}"
+
+
+@pytest.mark.parametrize("lens,window", [
+    ([1000], 0), ([1000], 1), ([1000], 127), ([1000], 128), ([1000], 129), ([1000], 300),
+    ([1000], 512), ([1000], 513), ([2048], 512), ([2048], 0),
+    ([129, 300, 1, 700], 256), ([129, 300, 1, 700], 0), ([128, 128, 255], 128)])
+def test_attention_prefill_mask_membership(lens, window):
+    nq, nkv = 4, 2
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    rng = np.random.default_rng(T + window)
+    q = torch.zeros(T, nq * 128, dtype=torch.bfloat16, device="cuda")
+    k = bf16_dev(rng.standard_normal((T, nkv * 128)))
+    vp = np.zeros((T, nkv, 128))
+    for s0, s1 in zip(cu[:-1], cu[1:]):
+        vp[s0:s1] = _onehot_by_position(s1 - s0, nkv)
+    v = bf16_dev(vp.reshape(T, nkv * 128))
+    out = torch.empty(T, nq * 128, dtype=torch.bfloat16, device="cuda")
+    L.cc_op_attention_prefill(q, k, v, out, nq * 128, torch.from_numpy(cu).cuda(), len(lens), T,
+                              nq, nkv, window)
+    _sync()
+    want = np.zeros((T, nq, 128))
+    for s0, s1 in zip(cu[:-1], cu[1:]):
+        for i in range(s1 - s0):
+            lo = max(0, i - window + 1) if window > 0 else 0
+            want[s0 + i] = _visible_fraction(lo, i)
+    got = f64(out).reshape(T, nq, 128)
+    _assert_one_rounding(got, want, f"prefill mask lens={lens} window={window}")
+    # the oracle's masks give the same visible sets
+    ref = O.attention(np.zeros((T, nq, 128)), f64(k).reshape(T, nkv, 128), vp, cu,
+                      window if window > 0 else None, 128 ** -0.5)
+    np.testing.assert_allclose(ref, want, rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("window", [0, 1, 16, 127, 128, 129, 1024, 4096])
+def test_attention_decode_mask_membership(window):
+    nq, nkv, ps = 8, 2, 16
+    n_keys = np.array([1, 15, 16, 17, 127, 128, 129, 1023, 1024, 1025, 4096, 4097],
+                      dtype=np.int32)
+    B = len(n_keys)
+    max_pages = (int(n_keys.max()) + ps - 1) // ps
+    n_pages = B * max_pages + 3
+    rng = np.random.default_rng(window + 11)
+    table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    vp = np.zeros((n_pages, nkv, ps, 128))
+    for b in range(B):
+        j = np.arange(int(n_keys[b]))
+        vp[table[b][j // ps], :, j % ps, j % 128] = 1.0
+    kp = bf16_dev(rng.standard_normal((n_pages, nkv, ps, 128)))
+    q = torch.zeros(B, nq * 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(B, nq * 128, dtype=torch.bfloat16, device="cuda")
+    L.cc_op_attention_decode(q, kp, bf16_dev(vp), n_pages, torch.from_numpy(table).cuda(),
+                             max_pages, torch.from_numpy(n_keys).cuda(), B, nq, nkv, ps, window,
+                             out, nq * 128)
+    _sync()
+    want = np.zeros((B, nq, 128))
+    for b in range(B):
+        n = int(n_keys[b])
+        lo = max(0, n - window) if window > 0 else 0
+        want[b] = _visible_fraction(lo, n - 1)
+    _assert_one_rounding(f64(out).reshape(B, nq, 128), want, f"decode mask window={window}")
+
+
 # --------------------------------------------------------------------------- decode attention
 @pytest.mark.parametrize("nq,nkv,window,max_pages", [
     (8, 2, 0, 44), (8, 2, 200, 44), (16, 4, 0, 44), (4, 4, 37, 44), (8, 1, 0, 44),

@@ -278,6 +278,18 @@ def test_attention_matches_elementwise_loops(window):
                     assert abs(out[i, h, c] - want) < 1e-12
 
 
+
+def test_attention_row_blocking_changes_nothing():
+    """The oracle evaluates query rows in blocks whose key range starts at the block's first
+    row minus the window; any block size gives every row the same visible keys."""
+    rng = np.random.default_rng(10)
+    q, k, v = _rand_qkv(rng, 45, 4, 2, 8)
+    for window in (None, 1, 6, 20):
+        a = O.attention(q, k, v, [0, 19, 45], window, 0.3, row_block=1024)
+        for rb in (1, 4, 7):
+            b = O.attention(q, k, v, [0, 19, 45], window, 0.3, row_block=rb)
+            np.testing.assert_allclose(a, b, atol=1e-14)
+
 def test_window_at_least_sequence_equals_full_causal():
     rng = np.random.default_rng(7)
     q, k, v = _rand_qkv(rng, 70, 4, 1, 16)
