@@ -27,6 +27,9 @@
  *    cc_sync / cc_op_sync returns; the results of the affected calls are undefined.
  *  - No call aborts the process or throws across the ABI.
  *  - bf16 tensors hold raw bfloat16 bit patterns; f32 tensors hold IEEE floats.
+ *  - A process drives the library on one CUDA device: each kernel's shared-memory limit
+ *    is configured once, on the device current at its first launch. Calls on one plan
+ *    come from one host thread at a time (they reuse the plan's workspace).
  */
 #ifndef CC_H_
 #define CC_H_
