@@ -13,7 +13,7 @@ namespace {
 // mlxcel issue "Cohere Compass / North-Micro-Vision", "Text decoder forward": LayerNorm
 // with weight only (no bias), statistics in f32; biased variance, eps inside the root.
 // One warp per row; two passes over the row (mean, then centred second moment) kept in
-// registers (H / 128 float4 per lane, H <= 128 * kMaxV4).
+// registers (H / 128 float4 per lane, any multiple of 128 up to 128 * kMaxV4).
 constexpr int kMaxV4 = 32;  // H <= 4096 in the register-resident variant
 
 // LayerNorm of one row held by a warp (lane owns columns 4 (lane + 32 i) .. +3, i < NV4):
@@ -138,8 +138,10 @@ cc_status launch_ln(const float* x, const void* gamma, OutT* out, int rows, int 
 #define CC_LN_CASE(N) \
   case N: e = launch_pdl(k_layernorm<N, OutT>, grid, dim3(256), 0, s, x, gamma, out, rows, H, eps, row_idx, gamma_bf16); break;
   switch (nv4) {
-    CC_LN_CASE(1) CC_LN_CASE(2) CC_LN_CASE(3) CC_LN_CASE(4) CC_LN_CASE(6) CC_LN_CASE(8)
-    CC_LN_CASE(12) CC_LN_CASE(16) CC_LN_CASE(24) CC_LN_CASE(32)
+    CC_LN_CASE(1) CC_LN_CASE(2) CC_LN_CASE(3) CC_LN_CASE(4) CC_LN_CASE(5) CC_LN_CASE(6) CC_LN_CASE(7) CC_LN_CASE(8)
+    CC_LN_CASE(9) CC_LN_CASE(10) CC_LN_CASE(11) CC_LN_CASE(12) CC_LN_CASE(13) CC_LN_CASE(14) CC_LN_CASE(15) CC_LN_CASE(16)
+    CC_LN_CASE(17) CC_LN_CASE(18) CC_LN_CASE(19) CC_LN_CASE(20) CC_LN_CASE(21) CC_LN_CASE(22) CC_LN_CASE(23) CC_LN_CASE(24)
+    CC_LN_CASE(25) CC_LN_CASE(26) CC_LN_CASE(27) CC_LN_CASE(28) CC_LN_CASE(29) CC_LN_CASE(30) CC_LN_CASE(31) CC_LN_CASE(32)
     default: return CC_ERR_UNSUPPORTED;
   }
 #undef CC_LN_CASE
@@ -314,8 +316,10 @@ cc_status launch_embed_ln(const int32_t* tok, const __nv_bfloat16* embed, int V,
                    rows, H, h, ln_w, eps, ln_out, err);                                    \
     break;
   switch (H / 128) {
-    CC_EMB_CASE(1) CC_EMB_CASE(2) CC_EMB_CASE(3) CC_EMB_CASE(4) CC_EMB_CASE(6) CC_EMB_CASE(8)
-    CC_EMB_CASE(12) CC_EMB_CASE(16) CC_EMB_CASE(24) CC_EMB_CASE(32)
+    CC_EMB_CASE(1) CC_EMB_CASE(2) CC_EMB_CASE(3) CC_EMB_CASE(4) CC_EMB_CASE(5) CC_EMB_CASE(6) CC_EMB_CASE(7) CC_EMB_CASE(8)
+    CC_EMB_CASE(9) CC_EMB_CASE(10) CC_EMB_CASE(11) CC_EMB_CASE(12) CC_EMB_CASE(13) CC_EMB_CASE(14) CC_EMB_CASE(15) CC_EMB_CASE(16)
+    CC_EMB_CASE(17) CC_EMB_CASE(18) CC_EMB_CASE(19) CC_EMB_CASE(20) CC_EMB_CASE(21) CC_EMB_CASE(22) CC_EMB_CASE(23) CC_EMB_CASE(24)
+    CC_EMB_CASE(25) CC_EMB_CASE(26) CC_EMB_CASE(27) CC_EMB_CASE(28) CC_EMB_CASE(29) CC_EMB_CASE(30) CC_EMB_CASE(31) CC_EMB_CASE(32)
     default: return CC_ERR_UNSUPPORTED;
   }
 #undef CC_EMB_CASE

@@ -162,3 +162,14 @@ def test_mrope_layout_argument_is_checked(lib):
     bad = L._i32_array((24, 20, 21))   # does not sum to head_dim / 2
     assert lib.cc_op_mrope_table_layout(256, 4, 128, 5e4, bad, 1, 256, None) == L.CC_ERR_INVALID_ARG
     assert lib.cc_op_mrope_table_layout(256, 0, 128, 5e4, section, 1, 256, None) == L.CC_OK
+
+
+def test_layernorm_widths_are_checked_before_any_device_work(lib):
+    """Every multiple of 128 up to 4096 is a supported row width; others are refused on the
+    host (the pointers below are never dereferenced)."""
+    dummy = 256
+    for H in (100, 4224, 8192):
+        assert lib.cc_op_layernorm(dummy, dummy, dummy, 4, H, 1e-5, None, None) == \
+            L.CC_ERR_UNSUPPORTED
+    assert lib.cc_op_layernorm(dummy, dummy, dummy, 0, 4096, 1e-5, None, None) == L.CC_OK
+    assert lib.cc_op_layernorm(dummy, dummy, dummy, 4, 0, 1e-5, None, None) == L.CC_ERR_INVALID_ARG

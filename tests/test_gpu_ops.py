@@ -28,7 +28,8 @@ def _sync():
 
 
 # --------------------------------------------------------------------------- LayerNorm
-@pytest.mark.parametrize("rows,H", [(300, 2048), (5, 256), (129, 1024)])
+@pytest.mark.parametrize("rows,H", [(300, 2048), (5, 256), (129, 1024), (1, 128), (33, 640),
+                                    (17, 4096), (9, 3968)])
 def test_layernorm_matches_oracle(rows, H):
     rng = np.random.default_rng(rows + H)
     x = (rng.standard_normal((rows + 7, H)) * 3 + 0.5).astype(np.float32)
@@ -46,7 +47,8 @@ def test_layernorm_matches_oracle(rows, H):
 
 
 # --------------------------------------------------------------------------- embedding merge
-@pytest.mark.parametrize("T,H,V,n_img", [(300, 256, 1000, 37), (1, 128, 7, 0), (513, 2048, 4000, 200)])
+@pytest.mark.parametrize("T,H,V,n_img", [(300, 256, 1000, 37), (1, 128, 7, 0), (513, 2048, 4000, 200),
+                                         (70, 640, 300, 9), (20, 4096, 50, 3)])
 def test_embed_merge_matches_oracle(T, H, V, n_img):
     rng = np.random.default_rng(T + H)
     embed = bf16_dev(0.5 * rng.standard_normal((V, H)))

@@ -97,6 +97,22 @@ def test_small_stack_with_empty_sequences():
     _check(inp, gw, h, lg)
 
 
+
+def test_small_stack_hidden_640_prefill_and_decode():
+    """A hidden size that is a multiple of 128 but not of 256 (640: five 128-column blocks per
+    LayerNorm row, 128-wide output tiles in the residual GEMM), through prefill, the head and a
+    decode step."""
+    inp = _small("small_h640", [200], [ImageSpan(0, 25, 1, 4, 6)], 1,
+                 types=(SLIDING, FULL), window=50, hidden=640, inter=320, seed=24)
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+    shape = small_shape(num_layers=2, layer_types=(SLIDING, FULL), window=70, hidden=640,
+                        inter=320)
+    dec = Inputs(Workload("dec_h640", shape, "decode", [], head_rows="all", seed=25,
+                          decode_batch=5, cache_len=90, page_size=16))
+    gw, h, lg = _run(dec)
+    _check(dec, gw, h, lg)
+
 def test_small_stack_mha_and_no_images():
     inp = _small("small3", [130], [], 0, types=(FULL, SLIDING), window=33, heads=(2, 2),
                  hidden=128, inter=128, vocab=256, seed=23)
