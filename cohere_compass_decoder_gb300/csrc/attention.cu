@@ -842,12 +842,8 @@ cc_status launch_attn_prefill(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               const int32_t* n_tiles, int max_tiles, int n_q, int n_kv,
                               int window, const AttnScratch& sc, int* err, cudaStream_t s,
                               const AttnPaged& paged) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    CC_CHECK_CUDA(cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmem)));
-    attr_set = true;
-  }
+  static std::atomic<bool> smem_set{false};
+  CC_CHECK_CUDA(allow_dynamic_smem(k_attn_prefill, kSmem, smem_set));
   if (max_tiles <= 0) return CC_OK;
   if (n_kv <= 0 || n_q % n_kv != 0) return CC_ERR_INVALID_ARG;
   if (!sc.part_o || !sc.part_ml || !sc.counters || !sc.sched) return CC_ERR_INVALID_ARG;

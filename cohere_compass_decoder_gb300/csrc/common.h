@@ -1,6 +1,7 @@
 // Shared constants and host helpers of the cc library (device-independent parts).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <utility>
@@ -64,6 +65,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` on its first launch in the process
+// (the library drives one device per process). Safe from several host threads: concurrent
+// first launches may both set the attribute, which is idempotent.
+template <typename... KArgs>
+cudaError_t allow_dynamic_smem(void (*kernel)(KArgs...), size_t bytes, std::atomic<bool>& done) {
+  if (done.load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(bytes));
+  if (e == cudaSuccess) done.store(true, std::memory_order_release);
+  return e;
 }
 
 }  // namespace cc

@@ -363,12 +363,8 @@ cc_status launch_dec(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
                      int n_pages, const int32_t* pt, int max_pages, const int32_t* n_keys,
                      int batch, int n_kv, int window, int splits, DecodeScratch scr, int* err,
                      cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    CC_CHECK_CUDA(cudaFuncSetAttribute(k_attn_decode<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmem)));
-    attr_set = true;
-  }
+  static std::atomic<bool> smem_set{false};
+  CC_CHECK_CUDA(allow_dynamic_smem(k_attn_decode<G>, kSmem, smem_set));
   const float sl2 = (1.0f / sqrtf(128.0f)) * kLog2e;
   dim3 grid(splits, n_kv, batch);
   CC_CHECK_CUDA(launch_pdl(k_attn_decode<G>, grid, dim3(kThreads), kSmem, s, tq, tk, tv, n_pages, pt,

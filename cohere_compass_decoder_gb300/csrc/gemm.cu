@@ -355,13 +355,9 @@ template <int BN, int EPI>
 cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
                    const EpiParams& ep, int* err, cudaStream_t s) {
   using C = GemmCfg<BN>;
-  static bool attr_set = false;
+  static std::atomic<bool> smem_set{false};
   auto kern = k_gemm<BN, EPI>;
-  if (!attr_set) {
-    CC_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::kSmem)));
-    attr_set = true;
-  }
+  CC_CHECK_CUDA(allow_dynamic_smem(kern, C::kSmem, smem_set));
   const int m_tiles = (M + kBM - 1) / kBM;
   const int units = m_tiles * (N / BN) * splits;
   const int grid = units < num_sms() ? units : num_sms();
@@ -834,13 +830,9 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 template <int EPI>
 cc_status launch_q4_t(const CUtensorMap& tx, const uint8_t* wt, int M, int BT, int N, int K,
                       int splits, const EpiParams& ep, int* err, cudaStream_t s) {
-  static bool attr_set = false;
+  static std::atomic<bool> smem_set{false};
   auto kern = k_gemm_q4<EPI>;
-  if (!attr_set) {
-    CC_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kQ4Smem)));
-    attr_set = true;
-  }
+  CC_CHECK_CUDA(allow_dynamic_smem(kern, kQ4Smem, smem_set));
   const int units = (N / kQ4Rows) * splits;
   const int grid = units < num_sms() ? units : num_sms();
   CC_CHECK_CUDA(launch_pdl(kern, dim3(grid), dim3(kQ4Threads), kQ4Smem, s, tx, wt, M, BT, N, K,
