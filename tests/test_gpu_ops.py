@@ -299,6 +299,8 @@ def _attn_case(lens, nq, nkv, window, seed, qscale=1.0, ramp=0.0):
     ([1], 2, 1, 0),
     ([1000], 16, 4, 512),
     ([129, 128, 127], 8, 1, 0),
+    ([300], 16, 1, 0),
+    ([260, 77], 16, 1, 100),
 ])
 def test_attention_prefill_matches_oracle(lens, nq, nkv, window):
     got, want = _attn_case(lens, nq, nkv, window, seed=sum(lens) + nq + window)
