@@ -60,3 +60,11 @@ def test_reference_arm_under_torchrun_prints_once(tmp_path):
     assert line["n_gpus"] == 2 and line["steps"] == 1
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the rest of the JSON-line contract
+    for key in ("metric", "unit", "ms_per_step", "higher_is_better", "scaling", "vs_baseline",
+                "dtype", "data", "config", "warmup"):
+        assert key in line, key
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["dtype"] == "f64" and line["vs_baseline"] is None
+    assert line["config"]["workload"] and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
