@@ -364,7 +364,7 @@ cc_status cc_op_embed_merge(const int32_t* token_ids, int32_t tokens, const void
 /* LayerNorm (Compass issue, "Text decoder forward": weight only, no bias, f32 statistics,
  * biased variance, eps inside the square root): out[r] = bf16(gamma * (x[src] - mean) /
  * sqrt(var + eps)), src = row_idx ? row_idx[r] : r. x f32 [*, H]; gamma bf16 [H];
- * out bf16 [rows, H]. H % 128 == 0. */
+ * out bf16 [rows, H]. H % 128 == 0 and H <= 4096 (else CC_ERR_UNSUPPORTED). */
 cc_status cc_op_layernorm(const float* x, const void* gamma, void* out, int32_t rows,
                           int32_t hidden, float eps, const int32_t* row_idx, void* stream);
 
