@@ -259,7 +259,18 @@ def layer_norm(x, gamma, eps):
 
 
 def silu(x):
+    """x * sigmoid(x) = x / (1 + e^-x), the SwiGLU gate activation (reading: the block's
+    "SwiGLU" is the usual silu-gated linear unit)."""
     return x / (1.0 + np.exp(-x))
+
+
+def swiglu(a, wg, wu, wd, rb=lambda x: x):
+    """The MLP branch of the block ([Compass issue] "Text decoder forward": mlp = SwiGLU(a)):
+    down_proj(silu(gate_proj(a)) * up_proj(a)), with gate_proj = ``wg``, up_proj = ``wu``,
+    down_proj = ``wd`` (output-major [out, in] matrices). ``rb`` rounds the gated product
+    before down_proj (bf16 in the mirror mode, where the GPU stores it)."""
+    act = rb(silu(a @ wg.T) * (a @ wu.T))
+    return act @ wd.T
 
 
 # ----------------------------------------------------------------------------------
@@ -331,8 +342,7 @@ def block(h, layer, layer_type, shape, cos_sin, cu_seqlens, mirror_bf16):
     q, k, v = rb(q), rb(k), rb(v)
     o = rb(attention(q, k, v, cu_seqlens, window, d ** -0.5))
     attn = o.reshape(T, nq * d) @ _w(layer, "wo").T
-    act = rb(silu(a @ _w(layer, "wg").T) * (a @ _w(layer, "wu").T))
-    mlp = act @ _w(layer, "wd").T
+    mlp = swiglu(a, _w(layer, "wg"), _w(layer, "wu"), _w(layer, "wd"), rb)
     return h + attn + mlp
 
 
@@ -415,8 +425,7 @@ def decode_step(hidden, layers, shape, seq_lens, rope_delta, page_table, kv, pag
                 o[b, hq, :] = (p / p.sum()) @ V[lo:, g, :]
         o = rb(o)
         attn = o.reshape(B, nq * d) @ _w(layer, "wo").T
-        act = rb(silu(a @ _w(layer, "wg").T) * (a @ _w(layer, "wu").T))
-        h = h + attn + act @ _w(layer, "wd").T
+        h = h + attn + swiglu(a, _w(layer, "wg"), _w(layer, "wu"), _w(layer, "wd"), rb)
     return h
 
 

@@ -406,6 +406,77 @@ def test_logits_linear_in_logit_scale():
     assert l1.shape == (24, 50)
 
 
+def test_silu_against_its_closed_form():
+    """silu(0) = 0; silu(x) - silu(-x) = x (x * (sigmoid(x) + sigmoid(-x)) = x); silu(1) =
+    sigmoid(1) = 1 / (1 + 1/e); silu(x) -> x for large x and -> 0 for very negative x.
+    A sigmoid, a gelu or a tanh gate fails at least one of these."""
+    assert O.silu(np.float64(0.0)) == 0.0
+    x = np.linspace(-30.0, 30.0, 6001)
+    np.testing.assert_allclose(O.silu(x) - O.silu(-x), x, rtol=0, atol=1e-13)
+    assert O.silu(np.float64(1.0)) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+    assert O.silu(np.float64(40.0)) == pytest.approx(40.0, rel=1e-15)
+    assert abs(O.silu(np.float64(-40.0))) < 1e-15
+
+
+def test_swiglu_branch_golden():
+    """The hand-worked SwiGLU example (tests/golden/swiglu_tiny.txt): gate and up read
+    different inputs, so their order is fixed."""
+    g = read_golden("swiglu_tiny.txt")
+    a = np.array([g["a"]])
+    wg, wu, wd = np.array([g["wg"]]), np.array([g["wu"]]), np.array([g["wd"]])
+    got = O.swiglu(a, wg, wu, wd)
+    assert got.shape == (1, 1)
+    assert got[0, 0] == pytest.approx(g["swiglu"][0], rel=1e-15)
+    assert abs(got[0, 0] - g["swapped"][0]) > 0.2
+
+
+def test_block_swiglu_golden():
+    """One whole block on the hand-worked input of tests/golden/swiglu_tiny.txt: attention
+    weights zero, so the block adds exactly the SwiGLU branch of a = LayerNorm(h). Fails if
+    the block swaps gate and up, or gates with sigmoid instead of silu."""
+    g = read_golden("swiglu_tiny.txt")
+    shape = {"num_attention_heads": 1, "num_key_value_heads": 1, "head_dim": 2,
+             "layer_norm_eps": 0.0, "sliding_window": 4}
+    z = np.zeros((2, 2))
+    layer = {"ln": np.ones(2), "wq": z, "wk": z, "wv": z, "wo": z,
+             "wg": np.array([[1.0, 0.0]]), "wu": np.array([[0.0, 1.0]]),
+             "wd": np.array([[1.0], [0.0]])}
+    h = np.array([g["block_h"]])
+    out = O.block(h, layer, FULL, shape, None, [0, 1], False)
+    np.testing.assert_allclose(out[0], g["block_out"], rtol=0, atol=1e-15)
+    for wrong in ("block_swapped", "block_sigmoid"):
+        assert np.abs(out[0] - np.array(g[wrong])).max() > 0.4
+    # the decode step runs the same branch: one cached-free token, same result
+    kv = np.zeros((1, 1, 16, 2), np.float64)
+    dec = O.decode_step(h, [layer], dict(shape, num_layers=1, layer_types=(FULL,),
+                                         rope_theta=1e4, mrope_section=(1, 0, 0),
+                                         mrope_layout="interleaved"),
+                        [0], [0], np.zeros((1, 1), np.int64), lambda i: (kv, kv), 16, False)
+    np.testing.assert_allclose(dec[0], g["block_out"], rtol=0, atol=1e-15)
+
+
+def test_head_final_layer_norm_golden():
+    """The head on the hand-worked input of tests/golden/head_final_ln_tiny.txt: the final
+    LayerNorm (with its own gain) runs before the tied embedding and the logit_scale footer.
+    Fails if the norm is dropped or its gain ignored."""
+    g = read_golden("head_final_ln_tiny.txt")
+    h = np.array([g["h"]])
+    embed = np.array([g["embed_row0"], g["embed_row1"], g["embed_row2"]])
+    shape = {"layer_norm_eps": 0.0, "logit_scale": g["logit_scale"][0]}
+    for mirror in (False, True):    # every value on this path is exact in bf16
+        got = O.logits(h, np.array(g["final_ln"]), embed, shape, mirror)
+        np.testing.assert_array_equal(got[0], g["logits"])
+    for wrong in ("logits_no_final_ln", "logits_no_gain"):
+        assert np.abs(got[0] - np.array(g[wrong])).max() >= 0.25
+    # with the workloads' eps = 1e-5, a row of mean 0 and variance 1 scales by 1/sqrt(1 + eps)
+    eps = 1e-5
+    row = np.array([[-1.0, 1.0, -1.0, 1.0]])
+    got = O.logits(row, np.array(g["final_ln"]), embed, dict(shape, layer_norm_eps=eps), False)
+    gam = np.array(g["final_ln"])
+    want = g["logit_scale"][0] * np.array([gam[1], -gam[2], -gam[0] + gam[3]]) / math.sqrt(1 + eps)
+    np.testing.assert_allclose(got[0], want, rtol=1e-14)
+
+
 def test_text_prefill_is_causal():
     """First 48 logits of a 96-token prefill equal a 48-token prefill (4 layers, 3 sliding
     and 1 full), as in the pages' text_prefill_is_causal test."""
