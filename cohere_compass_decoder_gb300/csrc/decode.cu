@@ -320,6 +320,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           part_ml[pb2 * 2 + 1] = red[hh] + red[16 + hh] + red[32 + hh] + red[48 + hh];
         }
       }
+    } else if (t == 0) {
+      // a bounded wait gave up: the split counts as empty, so that the combine never merges
+      // a partial that an earlier launch left in the scratch
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const size_t pb2 = part_base + (size_t)hh * splits;
+        part_ml[pb2 * 2 + 0] = -INFINITY;
+        part_ml[pb2 * 2 + 1] = 0.f;
+      }
     }
   }
   __syncthreads();
@@ -419,8 +428,10 @@ cc_status launch_attn_decode(const __nv_bfloat16* q, int ld_q, const __nv_bfloat
 
 // ------------------------------------------------------------ no-allocation variant
 // Fixed split-KV scratch for callers that cannot allocate: 4 Mi floats (16 MiB) per GPU.
-// Every split either writes its partial (max, sum, O) or marks itself empty (max = -inf),
-// and the combine reads only the splits of the current call, so nothing needs clearing.
+// Every split of a call either writes its partial (max, sum, O) or marks itself empty
+// (max = -inf): when it has no keys in view, and when one of its bounded waits gave up (the
+// launch then also reports CC_ERR_TIMEOUT through err_flag, when one is given). The combine
+// reads only the splits of the current call, so nothing needs clearing between calls.
 constexpr size_t kNoAllocScratchFloats = size_t(1) << 22;
 constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];

@@ -435,7 +435,9 @@ cc_status cc_op_sync(void* stream);
  * the array, so calls that may overlap on the GPU (other streams, other threads) race and
  * must be serialised by the caller. err_flag: optional caller-owned device int32 that
  * receives CC_ERR_TIMEOUT / CC_ERR_DEVICE_CHECK (first error wins; the caller clears it);
- * NULL: device-side problems are not reported. */
+ * NULL: device-side problems are not reported. A split whose bounded wait gave up counts as
+ * empty (it never merges a partial left in the array by an earlier call), so the output of
+ * a call that reported CC_ERR_TIMEOUT is wrong but holds nothing of another call. */
 cc_status cc_op_attention_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
                                          int32_t n_pages, const int32_t* page_table,
                                          int32_t max_pages, const int32_t* n_keys, int32_t batch,

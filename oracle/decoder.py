@@ -385,6 +385,23 @@ def gather_cache(pool, page_table_row, n_tokens, page_size):
     return from_storage(pool[pages, :, idx % page_size, :])        # [n, nkv, d]
 
 
+def decode_attention(q, K, V, window, scale):
+    """Attention of the newest of the L = K.shape[0] tokens of one sequence: q [nq, d] is
+    query index L - 1, K and V [L, nkv, d] its keys and values in position order. Key j is
+    visible iff (L - 1) - j < window (sliding layers) or always (full, window None); query head
+    h reads KV head h // (nq // nkv) ([Compass issue] "Text decoder forward")."""
+    L, nkv = K.shape[0], K.shape[1]
+    nq = q.shape[0]
+    lo = 0 if window is None else max(0, L - window)    # first key with (L - 1) - j < window
+    out = np.zeros((nq, V.shape[2]))
+    for hq in range(nq):
+        g = hq // (nq // nkv)
+        s = (K[lo:, g, :] @ q[hq, :]) * scale
+        p = np.exp(s - s.max())
+        out[hq] = (p / p.sum()) @ V[lo:, g, :]
+    return out
+
+
 def decode_step(hidden, layers, shape, seq_lens, rope_delta, page_table, kv, page_size,
                 mirror_bf16=True):
     """One new token per sequence. ``kv(i)`` returns layer i's (K, V) pools holding
@@ -417,12 +434,7 @@ def decode_step(hidden, layers, shape, seq_lens, rope_delta, page_table, kv, pag
             n = int(seq_lens[b])                 # the new token is query index n
             K = np.concatenate([gather_cache(kpool, page_table[b], n, page_size), k[b:b + 1]])
             V = np.concatenate([gather_cache(vpool, page_table[b], n, page_size), v[b:b + 1]])
-            lo = 0 if win is None else max(0, n - win + 1)    # first key with n - j < win
-            for hq in range(nq):
-                g = hq // (nq // nkv)
-                s = (K[lo:, g, :] @ q[b, hq, :]) * d ** -0.5
-                p = np.exp(s - s.max())
-                o[b, hq, :] = (p / p.sum()) @ V[lo:, g, :]
+            o[b] = decode_attention(q[b], K, V, win, d ** -0.5)
         o = rb(o)
         attn = o.reshape(B, nq * d) @ _w(layer, "wo").T
         h = h + attn + swiglu(a, _w(layer, "wg"), _w(layer, "wu"), _w(layer, "wd"), rb)
