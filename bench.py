@@ -4,18 +4,21 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 A step is one whole pass of the path over one batch of synthetic input: the layer stack
-and the tied head. `value` is prefill tokens/s on the two-layer pair workload (sliding
-layer with MRoPE + full NoPE layer, bf16, T = 2048 with one 16x16 image at token 300 and
-a deepstack add after layer 0, head on the last token over a 256000 vocabulary); the
-`decode` object is the batched decode step (64 sequences x 4096 cached tokens, paged KV,
-head on all 64 rows). Inputs are resident in HBM when the timed region starts; every
-step reads 1.3 GB of weights (more than the 129 MB L2), so no flush is needed. `e2e`
-repeats the prefill measurement with host buffers: the step's inputs are copied from
-pinned host memory and its logits copied back inside the timed region.
+and the tied head. `value` is prefill tokens/s on the 28-layer stack (3:1 sliding:full,
+bf16, T = 8192 with three 32x32 images, deepstack adds after layers 0-2, head on the last
+token over a 256000 vocabulary); `--prefill-workload pair|varlen` selects the two-layer
+pair (T = 2048) or the varlen packed prefill (T = 32768) instead. Extra keys carry the
+two-layer pair, the single fp32 layer (T = 128, a latency in microseconds) and the batched
+decode step (64 sequences x 4096 cached tokens, paged KV, head on all 64 rows), each with
+its kernels against their rooflines. Inputs are resident in HBM when the timed region
+starts; every step reads several GB of weights (more than the 129 MB L2), so no flush is
+needed. `e2e` repeats the prefill measurement with host buffers: the step's inputs are
+copied from pinned host memory and its logits copied back inside the timed region.
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU (the path
 does not shard within a step); value = tokens of all ranks / max time over ranks.
-`--impl reference` times the CPU oracle (fp64 NumPy) as the reference arm.
+`--impl reference` times the CPU oracle (fp64 NumPy) on a stated sample of the same
+workload as the reference arm.
 """
 from __future__ import annotations
 
@@ -31,20 +34,26 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s and decode tokens/s (1 GB300) + % of bf16 tensor / HBM roofline"
-PREFILL_DESC = ("two-layer pair (sliding+interleaved MRoPE, full NoPE), bf16, batch 1, "
-                "seq 2048, hidden 2048, 16/4 heads, head_dim 128, SwiGLU 8192, window 512, "
-                "one 16x16 image at token 300, deepstack [256,2048] after layer 0, tied head "
-                "on the last token, vocab 256000")
-PREFILL_WORKLOADS = {"pair": "pair_T2048", "stack28": "stack28_T8192", "varlen": "varlen_T32768"}
-PREFILL_OTHER = {
-    "stack28": ("28-layer stack (full attention at every 4th layer), bf16, batch 1, seq 8192, window "
-        "4096, three 32x32 images, deepstack after layers 0-2, tied head on the last token"),
+PREFILL_WORKLOADS = {"stack28": "stack28_T8192", "pair": "pair_T2048", "varlen": "varlen_T32768"}
+_SHAPES = ("hidden 2048, 16/4 heads, head_dim 128, SwiGLU 8192, interleaved MRoPE [24,20,20], "
+           "theta 50000")
+PREFILL_DESC = {
+    "stack28": ("28-layer prefill stack (3:1 sliding:full, full NoPE at every 4th layer), bf16, "
+                "batch 1, seq 8192, " + _SHAPES + ", window 4096, three 32x32 images, deepstack "
+                "[3072,2048] after layers 0-2, tied head on the last token, vocab 256000, "
+                "logit_scale 0.0625"),
+    "pair": ("two-layer pair (sliding+interleaved MRoPE, full NoPE), bf16, batch 1, seq 2048, "
+             + _SHAPES + ", window 512, one 16x16 image at token 300, deepstack [256,2048] "
+             "after layer 0, tied head on the last token, vocab 256000"),
     "varlen": ("two-layer pair, varlen packed prefill of 4096/8192/12288/8192 tokens (T = 32768), "
-        "window 4096, 1-4 images per sequence, deepstack after layers 0-1, head on the last "
-        "token of each sequence"),
+               + _SHAPES + ", window 4096, 1-4 images per sequence, deepstack after layers "
+               "0-1, head on the last token of each sequence"),
 }
 DECODE_DESC = ("decode step on the two-layer pair: 64 sequences x 4096 cached bf16 tokens in "
                "16-token pages (permuted page table), window 4096, head on all 64 rows")
+# tokens of the oracle's sample (the first tokens of the workload's sequence, every layer and
+# the head): sized for roughly 5-15 s of fp64 work per pass on the GPU machine's host cores
+CPU_SAMPLE_TOKENS = {"stack28": 512, "pair": 2048, "varlen": 2048}
 
 
 def parse():
@@ -59,10 +68,15 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-q4", action="store_true", help="skip the 4-bit weight decode timing")
     p.add_argument("--cpu-tokens", type=int, default=0,
-                   help="oracle sample: first N tokens of the prefill workload (0: all)")
-    p.add_argument("--prefill-workload", choices=["pair", "stack28", "varlen"], default="pair",
-                   help="prefill workload: pair = two-layer pair T=2048 (the headline), "
-                        "stack28 = 28-layer stack T=8192, varlen = varlen packed T=32768")
+                   help="oracle sample: first N tokens of the prefill workload (0: the default "
+                        "sample of the workload)")
+    p.add_argument("--prefill-workload", choices=["stack28", "pair", "varlen"], default="stack28",
+                   help="prefill workload: stack28 = 28-layer stack T=8192 (the headline), "
+                        "pair = two-layer pair T=2048, varlen = varlen packed T=32768")
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling only: keep the first N layers of the workload (0: all)")
+    p.add_argument("--no-context", action="store_true",
+                   help="skip the extra workloads (two-layer pair, fp32 layer)")
     return p.parse_args()
 
 
@@ -77,9 +91,9 @@ def peaks():
 
 
 # ------------------------------------------------------------------------------ traffic
-# DRAM bytes per launch of a kernel from an ncu capture, kept in profiles/traffic.json with a
-# hash of the sources the kernel is built from; reported only while those sources are
-# unchanged since the capture.
+# DRAM bytes per launch of a kernel on a workload, from an ncu capture, kept in
+# profiles/traffic.json under "<kernel>@<workload>" with a hash of the sources the kernel is
+# built from; reported only while those sources are unchanged since the capture.
 KERNEL_SOURCES = {
     "gemm_qkv_mlp": ["gemm.cu", "ptx.cuh", "kernels.h", "common.h"],
     "attn_decode": ["decode.cu", "ptx.cuh", "kernels.h", "common.h"],
@@ -95,12 +109,12 @@ def sources_sha256(kernel):
     return h.hexdigest()
 
 
-def measured_traffic(kernel):
+def measured_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
+        rec = json.load(f).get(f"{kernel}@{workload}")
     if not rec or rec.get("sources_sha256") != sources_sha256(kernel):
         return None
     return rec["dram_bytes_per_launch"]
@@ -223,15 +237,35 @@ def kernel_profile(gw, fn, steps, base):
 
 
 # ------------------------------------------------------------------------------ legs
-def prefill_leg(args, dist, pk):
-    import numpy as np
+def make_workload(key, layers=0):
+    """The named prefill workload, optionally cut to its first `layers` layers (profiling)."""
+    import dataclasses
+    from synth.configs import WORKLOADS
+    wl = WORKLOADS[PREFILL_WORKLOADS[key]]()
+    if layers and layers < wl.shape.num_layers:
+        shape = dataclasses.replace(wl.shape, num_layers=layers,
+                                    layer_types=wl.shape.layer_types[:layers])
+        wl = dataclasses.replace(wl, shape=shape, n_deepstack=min(wl.n_deepstack, layers))
+    return wl
+
+
+def weight_bytes(shape):
+    """Bytes of the layer weights and of the tied head that one prefill step reads."""
+    H, d, I = shape.hidden_size, shape.head_dim, shape.intermediate_size
+    N1 = (shape.num_attention_heads + 2 * shape.num_key_value_heads) * d + 2 * I
+    K2 = shape.num_attention_heads * d + I
+    return shape.num_layers * (N1 * H + H * K2) * 2, shape.vocab_size * H * 2
+
+
+def prefill_leg(args, dist, pk, key, context=False):
+    """The prefill + head of workload `key`: K timed steps, then the per-kernel profile.
+    context=True: a shorter run for the extra keys (no e2e, no next rows)."""
     import torch
     from synth import Inputs
-    from synth.configs import pair_T2048
     from cohere_compass_decoder_gb300.workload import GpuWorkload
 
-    from synth.configs import WORKLOADS
-    inp = Inputs(WORKLOADS[PREFILL_WORKLOADS[args.prefill_workload]]())
+    wl = make_workload(key, 0 if context else args.layers)
+    inp = Inputs(wl)
     gw = GpuWorkload(inp)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
@@ -253,9 +287,14 @@ def prefill_leg(args, dist, pk):
     ach = flops / (g1["avg_us"] * 1e-6) / 1e12 if g1 else None
     roof = {"kernel": "gemm_qkv_mlp", "bound": "tensor", "achieved": ach, "peak": pk["bf16"],
             "unit": "TFLOP/s", "frac": (ach / pk["bf16"]) if ach else None,
-            "traffic": measured_traffic("gemm_qkv_mlp") if args.prefill_workload == "pair" else None,
-            "peak_source": f"{pk['src']} bf16 burst (of {pk['src']})",
+            "frac_of_sustained": (ach / pk["bf16_sus"]) if ach else None,
+            "traffic": None if args.layers else measured_traffic("gemm_qkv_mlp", wl.name),
+            "peak_source": f"bf16 burst (of {pk['src']}); frac_of_sustained: against the "
+                           f"sustained {pk['bf16_sus']} TFLOP/s (of {pk['src']})",
             "algorithmic_per_launch": f"2*T*N1*H = {flops:.4g} FLOP"}
+    if g1:
+        g1["tflops"] = ach
+        g1["frac_of_bf16_peak"] = ach / pk["bf16"]
     # other classes against their own roofs
     g2 = kern.get("gemm_out_resid")
     if g2:
@@ -268,21 +307,57 @@ def prefill_leg(args, dist, pk):
         fa = attn_flops(inp) / at["launches_per_step"]
         at["tflops"] = fa / (at["avg_us"] * 1e-6) / 1e12
         at["frac_of_bf16_peak"] = at["tflops"] / pk["bf16"]
+    gh = kern.get("gemm_head")
+    if gh:
+        hb = s.vocab_size * s.hidden_size * 2 + len(inp.head_rows) * s.vocab_size * 4
+        gh["gbs"] = hb / (gh["avg_us"] * 1e-6) / 1e9
+        gh["frac_of_hbm"] = gh["gbs"] / pk["hbm"]
     value = T * K * dist.world / (ms / 1e3)
     launches = sum(v["launches_per_step"] for v in kern.values())
     extra = kern.get("row_maps", {}).get("launches_per_step", 0) and 1  # ds map: fill + scatter
     res = dict(ms=ms, value=value, kernels=kern, roofline=roof,
                launches=int(round((launches + extra) * K)), tokens=T,
-               batch=len(inp.wl.seq_lens))
-    if s.dtype == "bf16":
+               batch=len(inp.wl.seq_lens), workload=wl.name, shape=s)
+    if s.dtype == "bf16" and context:
         res["next_rows"] = {"embed_merge_ln": embed_merge_timing(inp, gw, pk)}
-        if args.prefill_workload == "pair":
+        if key == "pair":
             res["next_rows"]["chunked_prefill"] = chunked_prefill_timing(inp, gw, pk)
     # e2e through host buffers
-    if not args.no_e2e:
+    if not args.no_e2e and not context:
         res["e2e"] = prefill_e2e(gw, inp, K, W, dist, stream)
     gw.close()
     return res
+
+
+def fp32_layer_latency(args):
+    """The single fp32 layer (T = 128) and its head, a latency: microseconds per step with
+    CUDA events over the timed steps (inputs resident)."""
+    import torch
+    from synth import Inputs
+    from synth.configs import layer_fp32_T128
+    from cohere_compass_decoder_gb300.workload import GpuWorkload
+    inp = Inputs(layer_fp32_T128())
+    gw = GpuWorkload(inp)
+    steps, warm = max(args.steps, 20), max(args.warmup, 3)
+    pool = [gw.fresh_hidden() for _ in range(steps + warm)]
+    logits = torch.empty(len(inp.head_rows), inp.shape.vocab_size, device="cuda")
+    for i in range(warm):
+        gw.step(pool[i], logits)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        gw.step(pool[warm + i], logits)
+    e1.record()
+    torch.cuda.synchronize()
+    gw.sync()
+    gw.close()
+    us = 1000.0 * e0.elapsed_time(e1) / steps
+    return {"workload": "single sliding layer, fp32, batch 1, seq 128, hidden 256, 4/1 heads, "
+                        "head_dim 64, SwiGLU 512, window 32, MRoPE [12,10,10], head over 1024 "
+                        "rows x 128 tokens",
+            "us_per_step": us, "tokens_per_s": 128 / (us * 1e-6), "steps": steps,
+            "note": "a latency: the layer stack and head launched back to back, CUDA events"}
 
 
 def embed_merge_timing(inp, gw, pk, iters=20):
@@ -524,7 +599,7 @@ def decode_leg(args, dist, pk):
     ach = per_launch / (ad["avg_us"] * 1e-6) / 1e9 if ad else None
     roof = {"kernel": "attn_decode", "bound": "hbm", "achieved": ach, "peak": pk["hbm"],
             "unit": "GB/s", "frac": (ach / pk["hbm"]) if ach else None,
-            "traffic": measured_traffic("attn_decode"),
+            "traffic": measured_traffic("attn_decode", inp.wl.name),
             "peak_source": f"HBM copy (of {pk['src']})",
             "algorithmic_per_launch": f"K+V of the visible keys, {per_launch:.4g} B"}
     gh = kern.get("gemm_head")
@@ -642,52 +717,103 @@ def decode_q4_timing(inp, gw, pk, steps=10):
                     "4096 cached tokens each); gbs counts the 4-bit weight stream only"}
 
 
-def cpu_baseline(args, tokens=0):
-    """The oracle (fp64 NumPy, as it stands) on the prefill workload or its first tokens."""
-    import numpy as np
-    from synth import Inputs
-    from synth.configs import pair_T2048, Workload
-    from oracle import runs
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
 
-    wl = pair_T2048()
-    if tokens and tokens < wl.total_tokens:
-        imgs = [i for i in wl.images if i.start + i.n_tokens <= tokens]
-        wl = Workload(wl.name + f"_first{tokens}", wl.shape, "prefill", [tokens], images=imgs,
-                      n_deepstack=wl.n_deepstack if imgs else 0, head_rows="last", seed=wl.seed)
+
+def cpu_sample(key, tokens=0):
+    """The oracle's sample of prefill workload `key`: its first `tokens` tokens (0: the
+    default sample size) through every layer and the head. Causal attention makes these rows
+    of the stack identical to the same rows of the whole prefill; images are kept when they
+    lie wholly inside the sample."""
+    import dataclasses
+    wl = make_workload(key)
+    tokens = tokens or CPU_SAMPLE_TOKENS[key]
+    if len(wl.seq_lens) > 1 or tokens >= wl.total_tokens:
+        return wl, f"the whole workload ({wl.total_tokens} tokens)"
+    imgs = [i for i in wl.images if i.start + i.n_tokens <= tokens]
+    wl = dataclasses.replace(wl, name=wl.name + f"_first{tokens}", seq_lens=[tokens],
+                             images=imgs, n_deepstack=wl.n_deepstack if imgs else 0)
+    return wl, (f"the first {tokens} of the {sum(make_workload(key).seq_lens)} tokens "
+                f"({len(imgs)} image(s) inside), every layer and the head")
+
+
+def cpu_baseline(args, key):
+    """The oracle (fp64 NumPy, as it stands) on a sample of prefill workload `key`; returns
+    the line's cpu_baseline object and the pass's seconds."""
+    from synth import Inputs
+    from oracle import runs
+    wl, what = cpu_sample(key, args.cpu_tokens)
     inp = Inputs(wl)
     for i in range(wl.shape.num_layers):
         inp.layer(i)
     _ = inp.embed
+    _ = inp.hidden
     t0 = time.perf_counter()
     runs.run_prefill(inp)
     dt = time.perf_counter() - t0
-    return {"value": wl.total_tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(),
-            "kind": "oracle", "seconds": dt,
-            "sample": f"one prefill + head of {wl.total_tokens} tokens of the prefill workload "
-                      f"(fp64 NumPy, BLAS on all host cores)"}
+    return {"value": wl.total_tokens / dt, "unit": "tokens/s", "cores": host_cores(),
+            "kind": "oracle",
+            "sample": f"one oracle prefill + head over {what} (fp64 NumPy, BLAS on all host "
+                      f"cores, inputs drawn before the clock starts)"}, dt
+
+
+def cpu_baseline_decode():
+    """The oracle's decode step + head on the whole decode workload (64 sequences)."""
+    from synth import Inputs
+    from synth.configs import decode_B64_cache4096
+    from oracle import runs
+    inp = Inputs(decode_B64_cache4096())
+    for i in range(inp.shape.num_layers):
+        inp.layer(i)
+        inp.kv(i)
+    _ = inp.embed
+    _ = inp.hidden
+    t0 = time.perf_counter()
+    runs.run_decode(inp)
+    dt = time.perf_counter() - t0
+    B = inp.wl.decode_batch
+    return {"value": B / dt, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"one oracle decode step + head over all {B} sequences (4096 cached "
+                      f"tokens each, both layers; fp64 NumPy, BLAS on all host cores)"}
+
+
+def line_config(args, world):
+    """The `config` of the JSON line, the same for both arms."""
+    wl = make_workload(args.prefill_workload, args.layers)
+    wb, hb = weight_bytes(wl.shape)
+    cfg = {"workload": wl.name + ": " + PREFILL_DESC[args.prefill_workload],
+           "global_batch": len(wl.seq_lens) * world, "seq_len": wl.total_tokens,
+           "parallelism": "replicas" if world > 1 else "single",
+           "l2": f"inputs larger than L2: {wb / 1e9:.2f} GB of layer weights and a "
+                 f"{hb / 1e9:.2f} GB head read per step"}
+    if args.layers:
+        cfg["layers"] = wl.shape.num_layers
+    return cfg
 
 
 def run_reference(args):
-    dist_rank = int(os.environ.get("RANK", "0"))
-    if dist_rank != 0:
+    """The reference arm: the oracle on the host cores, each step one pass over the sample of
+    the prefill workload (rank 0 only; other ranks exit without work)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
         return 0
-    tokens = args.cpu_tokens
-    vals = []
+    secs, cpu = [], None
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(args, tokens)
+        cpu, dt = cpu_baseline(args, args.prefill_workload)
         if i >= args.warmup:
-            vals.append(r)
-    secs = sum(r["seconds"] for r in vals)
-    T = vals[0]["value"] * vals[0]["seconds"]
-    value = T * len(vals) / secs
+            secs.append(dt)
+    tokens = cpu_sample(args.prefill_workload, args.cpu_tokens)[0].total_tokens
+    value = tokens * len(secs) / sum(secs)
+    cpu["value"] = value
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * secs / len(vals), "higher_is_better": True,
+            "ms_per_step": 1000.0 * sum(secs) / len(secs), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": PREFILL_DESC, "global_batch": 1, "seq_len": 2048,
-                       "parallelism": "replicas"},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
-                             "kind": "oracle", "sample": vals[0]["sample"]},
+            "config": line_config(args, world), "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -708,39 +834,52 @@ def main():
     pk = peaks()
     clocks = Clocks(dist.local) if dist.rank == 0 else None
     t_start = time.time()
-    pre = None if args.no_prefill else prefill_leg(args, dist, pk)
+    pre = None if args.no_prefill else prefill_leg(args, dist, pk, args.prefill_workload)
+    ctx = {}
+    if not args.no_prefill and not args.no_context:
+        if args.prefill_workload != "pair":
+            ctx["pair"] = prefill_leg(args, dist, pk, "pair", context=True)
+        ctx["fp32"] = fp32_layer_latency(args)
     dec = None if args.no_decode else decode_leg(args, dist, pk)
     # keep the clock sampler running for at least ~1 s of GPU work
     if clocks and time.time() - t_start < 1.5:
         time.sleep(0.1)
     clk = clocks.stop() if clocks else None
-    cpu = None
+    cpu = cpu_dec = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args, args.cpu_tokens)
-        cpu.pop("seconds", None)
+        if pre is not None:
+            cpu, _ = cpu_baseline(args, args.prefill_workload)
+        if dec is not None:
+            cpu_dec = cpu_baseline_decode()
     if dist.rank == 0 and pre is None:
-        print(json.dumps({"decode": dec}))
+        print(json.dumps({"decode": dec, "cpu_baseline_decode": cpu_dec}, default=str))
     elif dist.rank == 0:
         line = {
             "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": PREFILL_DESC if args.prefill_workload == "pair" else
-                       PREFILL_OTHER[args.prefill_workload],
-                       "global_batch": pre["batch"], "seq_len": pre["tokens"],
-                       "parallelism": "replicas" if dist.world > 1 else "single",
-                       "l2": "inputs larger than L2 (1.3 GB of weights per step)"},
+            "data": "synthetic (seeded; random-init weights of the workload's shapes)",
+            "config": line_config(args, dist.world),
             "roofline": pre["roofline"], "cpu_baseline": cpu,
             "e2e": pre.get("e2e"), "gpu_launches": pre["launches"], "clocks": clk,
             "kernels": pre["kernels"],
         }
-        if pre.get("next_rows"):
-            line["next_rows"] = pre["next_rows"]
+        if "pair" in ctx:
+            c = ctx["pair"]
+            line["pair_T2048"] = {"workload": PREFILL_DESC["pair"], "value": c["value"],
+                                  "unit": "tokens/s", "ms_per_step": c["ms"] / args.steps,
+                                  "roofline": c["roofline"], "gpu_launches": c["launches"],
+                                  "kernels": c["kernels"]}
+        for c in (pre, ctx.get("pair")):
+            if c and c.get("next_rows"):
+                line.setdefault("next_rows", {}).update(c["next_rows"])
+        if "fp32" in ctx:
+            line["layer_fp32_T128"] = ctx["fp32"]
         if dec:
             line["decode"] = {"workload": DECODE_DESC, "value": dec["value"], "unit": "tokens/s",
                               "ms_per_step": dec["ms"] / args.steps, "roofline": dec["roofline"],
-                              "gpu_launches": dec["launches"], "kernels": dec["kernels"]}
+                              "gpu_launches": dec["launches"], "kernels": dec["kernels"],
+                              "cpu_baseline": cpu_dec}
             if dec.get("next_rows"):
                 line.setdefault("next_rows", {}).update(dec["next_rows"])
         print(json.dumps(line))

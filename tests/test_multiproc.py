@@ -49,7 +49,7 @@ def test_reference_arm_under_torchrun_prints_once(tmp_path):
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port),
            os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
-           "--warmup", "0", "--cpu-tokens", "96"]
+           "--warmup", "0", "--cpu-tokens", "96", "--prefill-workload", "pair"]
     env = dict(os.environ, OMP_NUM_THREADS="1")
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
@@ -68,3 +68,35 @@ def test_reference_arm_under_torchrun_prints_once(tmp_path):
     assert line["dtype"] == "f64" and line["vs_baseline"] is None
     assert line["config"]["workload"] and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
+    # the same config dict as the GPU arm prints for these arguments
+    sys.path.insert(0, ROOT)
+    import bench
+    args = _parse(bench, cmd[cmd.index("--impl"):])
+    assert line["config"] == bench.line_config(args, 2)
+
+
+def _parse(bench, argv):
+    saved = sys.argv
+    sys.argv = ["bench.py"] + list(argv)
+    try:
+        return bench.parse()
+    finally:
+        sys.argv = saved
+
+
+def test_both_arms_name_the_same_stack28_workload_and_sample():
+    """The headline workload is the 28-layer T = 8192 stack; both arms build their config from
+    one function, and the oracle's default sample is a stated prefix of that sequence."""
+    sys.path.insert(0, ROOT)
+    import bench
+    args = _parse(bench, ["--impl", "reference"])
+    assert args.prefill_workload == "stack28"
+    cfg = bench.line_config(args, 1)
+    assert cfg["seq_len"] == 8192 and cfg["global_batch"] == 1 and cfg["parallelism"] == "single"
+    assert cfg["workload"].startswith("stack28_bf16_T8192: 28-layer")
+    assert "3.41 GB of layer weights" in cfg["l2"]
+    wl, what = bench.cpu_sample("stack28")
+    assert wl.shape.num_layers == 28 and wl.seq_lens == [bench.CPU_SAMPLE_TOKENS["stack28"]]
+    assert "every layer and the head" in what
+    wl4 = bench.make_workload("stack28", 4)
+    assert wl4.shape.num_layers == 4 and wl4.shape.layer_types[3] == "full_attention"
