@@ -184,6 +184,11 @@ struct cc_layer_plan {
   int32_t* attn_cnt = nullptr;
   size_t attn_cnt_ints = 0;
   int attn_groups_n = 1;
+  // the residual + LayerNorm epilogue: per-row partial statistics [T, H / 128] and one
+  // arrival counter per row block and layer (inside attn_cnt, zeroed before each forward)
+  float2* ln_part = nullptr;
+  int32_t* ln_cnt = nullptr;
+  int ln_row_blocks = 0;
   // tiled 4-bit affine weights (cc_layer_plan_attach_q4)
   std::vector<cc_layer_weights_q4> layers_q4;
   const void* embed_q4 = nullptr;
@@ -321,7 +326,11 @@ extern "C" cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_l
   parts.push_back({reinterpret_cast<void**>(&p->tiles_f), p->max_tiles * sizeof(AttnTile)});
   if (p->bf16) {
     p->attn_groups_n = attn_groups(p->nq, p->nkv);
-    p->attn_cnt_ints = (size_t)attn_counter_ints(p->attn_groups_n) + cfg->num_layers;
+    p->ln_row_blocks = (p->T_max + 127) / 128;
+    // [split counters | one item counter per layer | LayerNorm arrivals per layer, row block]
+    p->attn_cnt_ints = (size_t)attn_counter_ints(p->attn_groups_n) + cfg->num_layers +
+                       (size_t)cfg->num_layers * p->ln_row_blocks;
+    parts.push_back({reinterpret_cast<void**>(&p->ln_part), T * (p->H / 128) * sizeof(float2)});
     parts.push_back({reinterpret_cast<void**>(&p->attn_part_o),
                      attn_part_o_floats(p->nq, p->nkv) * sizeof(float)});
     parts.push_back({reinterpret_cast<void**>(&p->attn_part_ml),
@@ -356,6 +365,8 @@ extern "C" cc_status cc_layer_plan_create(const cc_model_config* cfg, const cc_l
     delete p;
     return CC_ERR_CUDA;
   }
+  if (p->bf16)
+    p->ln_cnt = p->attn_cnt + attn_counter_ints(p->attn_groups_n) + cfg->num_layers;
   if (p->bf16) {
     const int L = cfg->num_layers;
     p->w1_128.resize(L);
@@ -546,9 +557,14 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
       !make_tmap_bf16_2d(&tv, p->v, T, p->kv_cols, p->kv_cols, attn_kv_box_rows(), 64))
     return CC_ERR_CUDA;
   const int tiles = attn_max_tiles(T, n_seqs);
+  // the output projection's epilogue also normalises the updated rows for the next layer
+  const bool ln_fused = gemm_resid_ln_ok(T, p->H, p->K2);
   for (int i = 0; i < c.num_layers; ++i) {
     const bool sliding = p->types[i] == CC_SLIDING;
-    if (!(emb && i == 0))   // with token input, layer 0's LayerNorm ran with the merge
+    // layer 0's LayerNorm: with token input it ran with the embedding merge; later layers'
+    // ran in the previous layer's output projection when ln_fused
+    const bool a_ready = i == 0 ? emb != nullptr : ln_fused;
+    if (!a_ready)
       CC_TIMED(p, CC_K_LAYERNORM, s, launch_layernorm_bf16(hidden, static_cast<const __nv_bfloat16*>(p->layers[i].ln_w),
                                             p->a, T, p->H, c.layer_norm_eps, nullptr, s));
     EpiParams e1;
@@ -597,7 +613,16 @@ static cc_status prefill_bf16(cc_layer_plan* p, float* hidden, const int32_t* po
       e2.ds_map = p->ds_map;
       e2.ds = static_cast<const __nv_bfloat16*>(ds_feats[i]);
     }
-    CC_TIMED(p, CC_K_GEMM_OUT, s, plan_gemm(ta2, p->w2_128[i], p->w2_256[i], T, p->H, p->K2, EPI_RESID, e2,
+    int epi2 = EPI_RESID;
+    if (ln_fused && i + 1 < c.num_layers) {
+      epi2 = EPI_RESID_LN;
+      e2.ln_gamma = static_cast<const __nv_bfloat16*>(p->layers[i + 1].ln_w);
+      e2.ln_out = p->a;   // layer i + 1's GEMM-1 operand (layer i's GEMM-1 has read it)
+      e2.ln_part = p->ln_part;
+      e2.ln_cnt = p->ln_cnt + (size_t)i * p->ln_row_blocks;
+      e2.ln_eps = c.layer_norm_eps;
+    }
+    CC_TIMED(p, CC_K_GEMM_OUT, s, plan_gemm(ta2, p->w2_128[i], p->w2_256[i], T, p->H, p->K2, epi2, e2,
                               p->err, s));
   }
   return CC_OK;
@@ -1045,6 +1070,8 @@ extern "C" cc_status cc_op_attention_decode(const void* q, const void* k_pool, c
   CC_CHECK_CUDA(cudaFreeAsync(scratch, s));
   return st;
 }
+
+extern "C" void cc_test_stall_next_gemm(void) { test_stall_next_gemm(); }
 
 extern "C" cc_status cc_profile_enable(cc_layer_plan* p, int32_t enable) {
   if (!p) return CC_ERR_INVALID_ARG;

@@ -41,16 +41,70 @@ struct Unit {
   int mt, nt, kb0, kb1;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, int m_tiles, int n_tiles, int splits, int kbt) {
+// Unit u of a launch. m fastest (the default): CTAs running together share the weight tile.
+// n fastest (n_fast): the N / BN tiles of one row block are consecutive units, so that they
+// run at the same time on distinct CTAs (the residual + LayerNorm epilogue needs that).
+__device__ __forceinline__ Unit decode_unit(int u, int m_tiles, int n_tiles, int splits, int kbt,
+                                            bool n_fast = false) {
   Unit r;
   const int per_split = m_tiles * n_tiles;
   const int sp = u / per_split;
   const int rem = u - sp * per_split;
-  r.mt = rem % m_tiles;  // m fastest: CTAs running together share the weight tile
-  r.nt = rem / m_tiles;
+  if (n_fast) {
+    r.nt = rem % n_tiles;
+    r.mt = rem / n_tiles;
+  } else {
+    r.mt = rem % m_tiles;
+    r.nt = rem / m_tiles;
+  }
   r.kb0 = (kbt * sp) / splits;
   r.kb1 = (kbt * (sp + 1)) / splits;
   return r;
+}
+
+// The four epilogue warps (128 threads) synchronise at named barrier 1; __syncthreads uses 0.
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// The four epilogue warps agree on a predicate (AND) at barrier 1, so that all of them leave
+// or stay in the unit loop together and the exchange barriers stay matched.
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ float2 ld_cg_f2(const float2* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
+// Waits (bounded) until *cnt reaches `target`: the other output tiles of a row block, which
+// run at the same time on resident CTAs of this launch, count themselves there after storing.
+__device__ __forceinline__ bool wait_count(const int32_t* cnt, int target, int* err) {
+  const long long t0 = clock64();
+  for (uint32_t n = 0;; ++n) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) return true;
+    if ((n & 63u) == 63u) {
+      if (err && *reinterpret_cast<volatile int*>(err) != 0) return false;
+      if (clock64() - t0 > kWaitTimeoutCycles) {
+        set_error(err, CC_DEV_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(32);
+  }
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
@@ -200,6 +254,112 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, int n0, i
   }
 }
 
+// EPI_RESID_LN: the residual update of EPI_RESID followed by the next layer's LayerNorm of
+// the updated rows (mlxcel issue "Cohere Compass / North-Micro-Vision", "Text decoder
+// forward": a = LayerNorm(h), weight only, biased variance, eps inside the root, statistics
+// in f32). Pass 1 stores h += acc (+ deepstack) and this tile's (mean, M2) of the row over
+// its BN columns (Chan's update per 32-column chunk); the tile counts itself in its row
+// block's counter and waits (bounded) for the block's other N / BN tiles, which run at the
+// same time on other CTAs. Pass 2 merges the partials of the row (equal counts: mean = the
+// average of the means, M2 = sum M2_i + BN sum (mean_i - mean)^2), re-reads this tile's
+// columns of h and stores bf16((h - mean) * rstd * gamma). Returns false when the wait gave
+// up (every epilogue thread gets the same answer).
+template <int BN>
+__device__ __forceinline__ bool epilogue_resid_ln(uint32_t t_row, int row, int mt, int nt,
+                                                  int n_tiles, int M, const EpiParams& ep,
+                                                  int* err, volatile int* flag) {
+  const bool row_ok = row < M;
+  const int n0 = nt * BN;
+  const __nv_bfloat16* ds_row = nullptr;
+  if (ep.ds_map && row_ok) {
+    const int r = ep.ds_map[row];
+    if (r >= 0) ds_row = ep.ds + (size_t)r * ep.ldc;
+  }
+  float* hrow = ep.c + (size_t)row * ep.ldc + n0;
+  float mean = 0.f, m2 = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    float v[32];
+    tmem_ld32(t_row + c, v);
+    if (!row_ok) continue;
+    if (ds_row) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(ds_row + n0 + c + i);
+        v[i] += __bfloat162float(d2.x);
+        v[i + 1] += __bfloat162float(d2.y);
+      }
+    }
+    float4* d4 = reinterpret_cast<float4*>(hrow + c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 p = d4[i];
+      v[4 * i] += p.x;
+      v[4 * i + 1] += p.y;
+      v[4 * i + 2] += p.z;
+      v[4 * i + 3] += p.w;
+      d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sum += v[i];
+    const float mc = sum * (1.0f / 32.0f);
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float d = v[i] - mc;
+      q += d * d;
+    }
+    const float na = static_cast<float>(c), tot = na + 32.0f;
+    const float delta = mc - mean;
+    mean += delta * (32.0f / tot);
+    m2 += q + delta * delta * (na * 32.0f / tot);
+  }
+  if (row_ok) ep.ln_part[(size_t)row * n_tiles + nt] = make_float2(mean, m2);
+  __threadfence();
+  epi_bar();
+  if (threadIdx.x == 64) {   // the first epilogue thread counts the tile and waits
+    int32_t* cnt = ep.ln_cnt + mt;
+    atomicAdd(cnt, 1);
+    *flag = wait_count(cnt, n_tiles, err) ? 1 : 0;
+  }
+  epi_bar();
+  if (*flag == 0) return false;
+  if (row_ok) {
+    const float2* part = ep.ln_part + (size_t)row * n_tiles;
+    float sm = 0.f;
+#pragma unroll 1
+    for (int i = 0; i < n_tiles; ++i) sm += ld_cg_f2(part + i).x;
+    const float mu = sm / static_cast<float>(n_tiles);
+    float q = 0.f;
+#pragma unroll 1
+    for (int i = 0; i < n_tiles; ++i) {
+      const float2 pm = ld_cg_f2(part + i);
+      const float d = pm.x - mu;
+      q += pm.y + static_cast<float>(BN) * d * d;
+    }
+    const float rstd = rsqrtf(q / static_cast<float>(n_tiles * BN) + ep.ln_eps);
+    __nv_bfloat16* dst = ep.ln_out + (size_t)row * ep.ldc + n0;
+    const __nv_bfloat16* gam = ep.ln_gamma + n0;
+#pragma unroll 4
+    for (int c = 0; c < BN; c += 8) {
+      const float4 x0 = *reinterpret_cast<const float4*>(hrow + c);
+      const float4 x1 = *reinterpret_cast<const float4*>(hrow + c + 4);
+      const uint4 graw = __ldg(reinterpret_cast<const uint4*>(gam + c));
+      const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
+      const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
+      const float2 g2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.z));
+      const float2 g3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.w));
+      *reinterpret_cast<uint4*>(dst + c) = make_uint4(
+          pack_bf16x2((x0.x - mu) * rstd * g0.x, (x0.y - mu) * rstd * g0.y),
+          pack_bf16x2((x0.z - mu) * rstd * g1.x, (x0.w - mu) * rstd * g1.y),
+          pack_bf16x2((x1.x - mu) * rstd * g2.x, (x1.y - mu) * rstd * g2.y),
+          pack_bf16x2((x1.z - mu) * rstd * g3.x, (x1.w - mu) * rstd * g3.y));
+    }
+  }
+  return true;
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -219,6 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain = smem_u32(bars + 2 * S + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   int* consumed_slot = reinterpret_cast<int*>(bars + 2 * S + 6);
+  const uint32_t never = smem_u32(bars + 2 * S + 7);   // test hook: nothing arrives on it
+  volatile int* ln_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 8);
+  constexpr bool kNFast = EPI == EPI_RESID_LN;
 
   pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
@@ -237,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty0 + 8 * a, 128);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *consumed_slot = 0;
     fence_mbar_init();
   }
@@ -261,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt);
+        const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt, kNFast);
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, err)) {
             ok = false;
@@ -286,8 +450,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int iter = 0, consumed = 0;
       bool ok = true;
+      if (ep.test_stall) ok = mbar_wait(never, 0, err, kTestStallCycles);
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++iter) {
-        const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt);
+        const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt, kNFast);
         const int acc = iter & 1;
         if (!mbar_wait(tempty0 + 8 * acc, ((iter >> 1) & 1) ^ 1, err)) {
           ok = false;
@@ -327,13 +492,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     int iter = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++iter) {
-      const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt);
+      const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt, kNFast);
       const int acc = iter & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (iter >> 1) & 1, err))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int row = t.mt * kBM + quarter * 32 + lane;
-      epilogue_tile<BN, EPI>(t_row, row, t.nt * BN, M, t.kb0, splits, ep);
+      if constexpr (EPI == EPI_RESID_LN) {
+        if (!epilogue_resid_ln<BN>(t_row, row, t.mt, t.nt, n_tiles, M, ep, err, ln_flag)) break;
+      } else {
+        epilogue_tile<BN, EPI>(t_row, row, t.nt * BN, M, t.kb0, splits, ep);
+      }
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
     }
@@ -360,7 +529,14 @@ cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
   CC_CHECK_CUDA(allow_dynamic_smem(kern, C::kSmem, smem_set));
   const int m_tiles = (M + kBM - 1) / kBM;
   const int units = m_tiles * (N / BN) * splits;
-  const int grid = units < num_sms() ? units : num_sms();
+  int grid = units < num_sms() ? units : num_sms();
+  if (EPI == EPI_RESID_LN) {
+    // the N / BN tiles of a row block are consecutive units: with the grid a multiple of
+    // N / BN they run in the same round, each on its own CTA (one resident CTA per SM)
+    const int nt = N / BN;
+    if (nt > num_sms() || splits != 1) return CC_ERR_UNSUPPORTED;
+    grid = std::min(units, (num_sms() / nt) * nt);
+  }
   CC_CHECK_CUDA(launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmem, s, ta, tb, M, N, K, splits,
                           ep, err));
   return CC_OK;
@@ -413,25 +589,6 @@ constexpr uint32_t kQ4OffBar = kQ4OffEx + kQ4ExBytes;
 constexpr uint32_t kQ4Bars = 2 * kQ4QStages + 2 * kQ4Groups + 2 * kQ4XMaxStages + 7;
 constexpr size_t kQ4Smem = 1024 + kQ4OffBar + kQ4Bars * 8 + 64;
 static_assert(kQ4Smem <= 232448, "shared memory of the 4-bit GEMM");
-
-__device__ __forceinline__ void epi_bar() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// The four epilogue warps agree on a predicate (AND) at barrier 1, so that all of them leave
-// or stay in the unit loop together and the exchange barriers stay matched.
-__device__ __forceinline__ bool epi_all(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v))
-      : "memory");
-  return r != 0;
-}
 
 __device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -864,22 +1021,39 @@ void gemm_choose(int M, int N, int K, int epi, int* bn, int* splits) {
   *splits = sp;
 }
 
+// The fused residual + LayerNorm epilogue replaces the plain residual one wherever that one
+// would run unsplit (several row tiles); a single row tile keeps its K splits (decode).
+bool gemm_resid_ln_ok(int M, int N, int K) {
+  int bn, splits;
+  gemm_choose(M, N, K, EPI_RESID, &bn, &splits);
+  return M > 0 && splits == 1 && N % bn == 0 && N / bn <= num_sms();
+}
+
+static std::atomic<int> g_test_stall_next{0};
+
+void test_stall_next_gemm() { g_test_stall_next.store(1); }
+
 cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int bn,
-                      int splits, int epi, const EpiParams& ep, int* err, cudaStream_t s) {
+                      int splits, int epi, const EpiParams& ep_in, int* err, cudaStream_t s) {
   if (M <= 0) return CC_OK;
   if (K % kBK != 0 || N % bn != 0 || splits < 1 || splits > K / kBK)
     return CC_ERR_INVALID_ARG;
+  EpiParams ep = ep_in;
+  if (g_test_stall_next.load(std::memory_order_relaxed) && g_test_stall_next.exchange(0))
+    ep.test_stall = 1;
   if (bn == 256) {
     switch (epi) {
       case EPI_F32: return launch_t<256, EPI_F32>(ta, tb, M, N, K, splits, ep, err, s);
       case EPI_RESID: return launch_t<256, EPI_RESID>(ta, tb, M, N, K, splits, ep, err, s);
       case EPI_QKV_MLP: return launch_t<256, EPI_QKV_MLP>(ta, tb, M, N, K, 1, ep, err, s);
+      case EPI_RESID_LN: return launch_t<256, EPI_RESID_LN>(ta, tb, M, N, K, splits, ep, err, s);
     }
   } else if (bn == 128) {
     switch (epi) {
       case EPI_F32: return launch_t<128, EPI_F32>(ta, tb, M, N, K, splits, ep, err, s);
       case EPI_RESID: return launch_t<128, EPI_RESID>(ta, tb, M, N, K, splits, ep, err, s);
       case EPI_QKV_MLP: return launch_t<128, EPI_QKV_MLP>(ta, tb, M, N, K, 1, ep, err, s);
+      case EPI_RESID_LN: return launch_t<128, EPI_RESID_LN>(ta, tb, M, N, K, splits, ep, err, s);
     }
   }
   return CC_ERR_INVALID_ARG;

@@ -15,6 +15,7 @@ enum EpiMode : int {
   EPI_F32 = 0,      // c = alpha * acc (+ c)
   EPI_RESID = 1,    // h += acc (+ deepstack row)
   EPI_QKV_MLP = 2,  // column-typed: q / k / v heads (+ rotation, + paged K/V), SwiGLU
+  EPI_RESID_LN = 3, // EPI_RESID, then the next layer's LayerNorm of the updated rows
 };
 
 struct EpiParams {
@@ -41,6 +42,18 @@ struct EpiParams {
   int page_size = 16;
   __nv_bfloat16* act_out = nullptr;      // [M, ld_act]
   int ld_act = 0;
+  // EPI_RESID_LN: ln_out[row] = bf16(LayerNorm(h[row]) * ln_gamma) of the updated rows. Each
+  // output tile stores its rows' (mean, M2) over its columns in ln_part [M, N / BN] and counts
+  // itself in ln_cnt[m-tile] (zero when the launch starts; left at N / BN); the tiles of a
+  // row block meet there and each normalises its own columns.
+  const __nv_bfloat16* ln_gamma = nullptr;
+  __nv_bfloat16* ln_out = nullptr;       // [M, ldc]
+  float2* ln_part = nullptr;
+  int32_t* ln_cnt = nullptr;
+  float ln_eps = 0.f;
+  // test hook (cc_test_stall_next_gemm): the MMA thread first waits on a barrier that
+  // nothing arrives on, so the launch takes its timeout path
+  int test_stall = 0;
 };
 
 // C[M,N] (epilogue) = A[M,K] @ B[N,K]^T with A, B given by TMA maps (bf16, box 64 x 128
@@ -49,8 +62,14 @@ struct EpiParams {
 cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int bn,
                       int splits, int epi, const EpiParams& ep, int* err, cudaStream_t s);
 
+// Test hook: the next launch_gemm call (any thread) stalls its MMA thread (EpiParams::test_stall).
+void test_stall_next_gemm();
+
 // Picks bn / splits for a problem (used by every caller of launch_gemm).
 void gemm_choose(int M, int N, int K, int epi, int* bn, int* splits);
+// Whether launch_gemm runs EPI_RESID_LN for an [M, N] output (it needs one K split and an
+// output row block's N / bn tiles on distinct resident CTAs).
+bool gemm_resid_ln_ok(int M, int N, int K);
 
 // Tiled 4-bit affine weights of a [rows, K] matrix (rows % 128 == 0, K % 64 == 0): block
 // (t, j), t < rows / 128, j < ceil(K / 128), is kQ4TileBlockBytes contiguous bytes at
