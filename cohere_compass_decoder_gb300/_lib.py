@@ -27,7 +27,7 @@ EXPORTS = [
     "cc_kernel_class_name", "cc_op_attention_decode_noalloc", "cc_prefill_forward_tokens",
     "cc_op_embed_merge", "cc_prefill_forward_chunk", "cc_q4_tiled_bytes", "cc_pack_q4_tiles",
     "cc_pack_layer_weights_q4", "cc_layer_plan_attach_q4", "cc_decode_step_q4", "cc_logits_q4",
-    "cc_op_gemm_q4", "cc_op_mrope_table_layout",
+    "cc_op_gemm_q4", "cc_op_mrope_table_layout", "cc_test_stall_next_gemm",
 ]
 KERNEL_CLASSES = ["rope_table", "row_maps", "layernorm", "gemm_qkv_mlp", "attn_prefill",
                   "gemm_out_resid", "attn_decode", "gemm_head", "f32_path", "embed_merge"]
@@ -131,6 +131,7 @@ def lib() -> C.CDLL:
             "cc_profile_enable": (C.c_int, [vp, i32]),
             "cc_profile_read": (C.c_int, [vp, C.POINTER(cc_kernel_time)]),
             "cc_kernel_class_name": (C.c_char_p, [i32]),
+            "cc_test_stall_next_gemm": (None, []),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -345,6 +346,11 @@ def cc_logits_q4(plan, hidden, rows, n_rows, logits, stream=None):
 
 def cc_sync(plan, stream=None):
     _check(lib().cc_sync(plan, _stream(stream)), "cc_sync")
+
+
+def cc_test_stall_next_gemm():
+    """Test hook: the next bf16 GEMM launch takes its bounded-wait timeout path."""
+    lib().cc_test_stall_next_gemm()
 
 
 # ------------------------------------------------------------------------ single ops

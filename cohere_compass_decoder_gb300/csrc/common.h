@@ -15,9 +15,12 @@ namespace cc {
 // Device error codes written to the sticky error flag (same values as cc_status).
 enum : int { CC_DEV_TIMEOUT = CC_ERR_TIMEOUT, CC_DEV_CHECK = CC_ERR_DEVICE_CHECK };
 
-// A bounded inter-warp wait gives up after this many SM clock cycles (about 2 s at the
-// GB300's 2.07 GHz maximum clock; no launch here runs for seconds).
+// A bounded inter-warp wait gives up after this many SM clock cycles counted with clock64()
+// (about 1.9 s at the GB300's 2.07 GHz maximum clock, 2.7 s at 1.485 GHz; no launch here
+// runs for seconds).
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
+// The test hook's wait (cc_test_stall_next_gemm) gives up after this many cycles.
+constexpr long long kTestStallCycles = 100000000ll;
 
 constexpr int kNumSMsFallback = 152;
 

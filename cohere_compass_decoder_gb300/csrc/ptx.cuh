@@ -55,11 +55,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits until the phase of parity `parity` of the barrier has completed. Gives up, sets
-// *err = CC_DEV_TIMEOUT and returns false after about kWaitTimeoutCycles SM clocks, or
-// returns false early when *err is already set (another warp or an earlier launch gave
-// up), so that no warp of a failed launch waits forever. The common case (the phase
-// completes within a few hundred try_wait rounds) touches neither a timer nor memory.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+// *err = CC_DEV_TIMEOUT and returns false after about `limit` SM clocks (counted from the
+// end of the first 256 try_wait rounds), or returns false early when *err is already set
+// (another warp or an earlier launch gave up), so that no warp of a failed launch waits
+// forever. The common case (the phase completes within a few hundred try_wait rounds)
+// touches neither a timer nor memory.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
+                                          long long limit = kWaitTimeoutCycles) {
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -69,7 +71,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
     if (mbar_try_wait(bar, parity)) return true;
     if ((++n & 255u) == 0) {
       if (err && *reinterpret_cast<volatile int*>(err) != 0) return false;
-      if (clock64() - t0 > kWaitTimeoutCycles) {
+      if (clock64() - t0 > limit) {
         set_error(err, CC_DEV_TIMEOUT);
         return false;
       }

@@ -421,6 +421,15 @@ cc_status cc_op_attention_decode(const void* q, const void* k_pool, const void* 
  * single operations. */
 cc_status cc_op_sync(void* stream);
 
+/* Test hook of the device error path (the pages have no counterpart). The next bf16 tensor-
+ * core GEMM launched in this process, by any plan or single operation, starts with its MMA
+ * thread waiting on a barrier that nothing arrives on. That bounded wait gives up within
+ * about a second and records CC_ERR_TIMEOUT in the launch's error flag; the launch's other
+ * warps then stop waiting, its copies in flight land and its tensor memory is released, so
+ * the context stays usable. The call's outputs are wrong (cc_sync / cc_op_sync returns
+ * CC_ERR_TIMEOUT and clears the flag); later calls are unaffected. For tests only. */
+void cc_test_stall_next_gemm(void);
+
 /* Decode attention that allocates no device memory. The pages have no counterpart to
  * this call; it exists for callers that cannot call cudaMalloc: a serving runtime whose
  * memory pool has already reserved the device (a fresh allocation fails or fragments it),

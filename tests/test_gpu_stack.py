@@ -113,6 +113,30 @@ def test_small_stack_hidden_640_prefill_and_decode():
     gw, h, lg = _run(dec)
     _check(dec, gw, h, lg)
 
+def test_a_device_wait_that_runs_out_reports_timeout_and_the_plan_recovers():
+    """The bounded-wait error path on the GPU: the test hook makes the first GEMM of a forward
+    wait on a barrier that nothing arrives on. That wait gives up, cc_sync reports
+    CC_ERR_TIMEOUT (and clears the flag), and the next forward on the same plan is complete
+    and matches the oracle."""
+    inp = _small("small_stall", [260], [ImageSpan(0, 30, 1, 6, 6)], 1, seed=31)
+    gw = GpuWorkload(inp)
+    h = gw.fresh_hidden()
+    lg = gw.step(h)
+    gw.sync()
+    _check(inp, gw, h, lg)
+    L.cc_test_stall_next_gemm()
+    h_bad = gw.fresh_hidden()
+    gw.step(h_bad)
+    with pytest.raises(L.CCError) as e:
+        gw.sync()
+    assert e.value.status == L.CC_ERR_TIMEOUT
+    h2 = gw.fresh_hidden()
+    lg2 = gw.step(h2)
+    gw.sync()
+    _check(inp, gw, h2, lg2)
+    gw.close()
+
+
 def test_small_stack_mha_and_no_images():
     inp = _small("small3", [130], [], 0, types=(FULL, SLIDING), window=33, heads=(2, 2),
                  hidden=128, inter=128, vocab=256, seed=23)
