@@ -57,8 +57,7 @@ constexpr uint32_t kOffK = kOffQ + 2 * kTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTile;
 constexpr uint32_t kBarBytes = 256;                    // barriers, TMEM slot, item queue
-constexpr uint32_t kOffRed = kOffBar + kBarBytes;      // [2][2 halves][128 rows] fp32 maxima
-constexpr size_t kSmem = kOffRed + 2 * 2 * 128 * 4;   // the dynamic base is 1024-aligned
+constexpr size_t kSmem = kOffBar + kBarBytes;         // the dynamic base is 1024-aligned
 constexpr uint32_t kTmemCols = 512;  // head h: scores / P at 256 h, output at 256 h + 128
 constexpr uint32_t kIdescS = idesc_bf16(128, kKeys, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);
@@ -72,7 +71,7 @@ enum {
   B_KFULL, B_KEMPTY = B_KFULL + kKStages, B_VFULL = B_KEMPTY + kKStages,
   B_VEMPTY = B_VFULL + kVStages,
   B_SFULL = B_VEMPTY + kVStages,  // [head]: scores of the head's current tile ready
-  B_PFULL = B_SFULL + 2,          // [head], 256 arrivals: P of the head's current tile in TMEM
+  B_PFULL = B_SFULL + 2,          // [head], 128 arrivals: P of the head's current tile in TMEM
   B_ODONE = B_PFULL + 2,          // [head]: P V of the head's tiles
   B_IFULL = B_ODONE + 2,          // [2]: item queue entry written
   B_IEMPTY = B_IFULL + 2,         // [2], 1 + 8 arrivals: entry read by the MMA and softmax warps
@@ -197,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar(B_SFULL + h), 1);
-      mbar_init(bar(B_PFULL + h), 32 * kSoftmaxWarps);
+      mbar_init(bar(B_PFULL + h), 32 * kSoftmaxWarps / 2);
       mbar_init(bar(B_ODONE + h), 1);
       mbar_init(bar(B_IFULL + h), 1);
       mbar_init(bar(B_IEMPTY + h), 1 + kSoftmaxWarps);
@@ -358,18 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(B_DRAIN), 0, nullptr);
     }
   } else {
-    // ------------------------------------------------------------ softmax, all 8 warps
-    // Warp w takes keys 64*half .. 64*half+63 of every score tile (half = 0 for warps 2..5,
-    // 1 for warps 6..9) for the 32 query rows of its TMEM lane quarter; warps w and w+4 share
-    // those rows and combine their partial maxima through shared memory at a pair barrier.
-    // The heads of the item are processed one after the other, so each head's P is ready
-    // after half a tile's work while the tensor cores run the other head's products.
-    const int half = (warp - 2) >> 2;
+    // ------------------------------------------------------------ softmax, a group per head
+    // Warps 2..5 take head 0 of the item and warps 6..9 head 1 (the second group idles when
+    // the item has one head). Thread r of a group owns query row r (its TMEM lane) and all 128
+    // keys of every score tile, so a row's maximum, P and sum need no exchange between warps,
+    // and the two heads' softmax chains run side by side while the tensor cores alternate
+    // between the heads' products.
+    const int wg = (warp - 2) >> 2;                  // this group's head within the item
     const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;               // query row in the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int pair_bar = 3 + quarter;                // named barrier of warps (w, w+4)
-    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [2 buffers][2 halves][128 rows]
+    const uint32_t s_tmem = tmem + 256 * wg + lane_off;   // the head's scores, then its P
+    const uint32_t o_tmem = s_tmem + 128;                  // the head's output
     // All eight softmax warps take every decision to stop together, at a barrier that ANDs
     // their status, so none waits at a barrier another left.
     constexpr int kSmThreads = 32 * kSoftmaxWarps;
@@ -385,138 +384,109 @@ __global__ void __launch_bounds__(kThreads, 1)
       const AttnTile tile = tiles[u / groups];
       const int n = tile.kt1 - tile.kt0;
       const int head0 = (u % groups) * nh;
+      const bool active = wg < nh;                   // group-uniform
       const int q0 = tile.q0;
       const int qi = q0 + r;                         // query row among the call's tokens
       const int qa = tile.prefix + qi;               // its position: the key index it sees up to
       // this warp's rows that lie inside the sequence (rows past its end are never stored)
       const int qw_lo = tile.prefix + q0 + quarter * 32;
       const int qw_hi = tile.prefix + min(q0 + quarter * 32 + 31, tile.seq_len - 1);
-      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // l: this half's keys
-      for (int t = 0; t < n && ok; ++t) {
+      float m = -INFINITY, l = 0.f;
+      for (int t = 0; t < n && ok && active; ++t) {
         const int g = gt + t;
-        const int kbase = (tile.kt0 + t) * kKeys + 64 * half;     // first key of this half
-        // warp-uniform: every key of this half visible to every row of this warp
-        const bool full = (kbase + 63 <= qw_lo) && (window <= 0 || qw_hi - kbase < window);
+        const int kbase = (tile.kt0 + t) * kKeys;                // first key of the tile
+        // warp-uniform: every key of the tile visible to every row of this warp
+        const bool full = (kbase + kKeys - 1 <= qw_lo) && (window <= 0 || qw_hi - kbase < window);
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + wg), g & 1, err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float s[128];
+        tmem_ld128(s_tmem, s);
+        if (!full) {
+          const int hi_c = qa - kbase;                           // causal: c <= hi_c
+          const int lo_c = window > 0 ? qa - window + 1 - kbase : -1;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h >= nh) break;
-          const uint32_t s_tmem = tmem + 256 * h + lane_off;
-          const uint32_t o_tmem = s_tmem + 128 + 64 * half;
-          const bool w_ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + h), g & 1, err));
-          float* rb = red + (nh == 2 ? h : (g & 1)) * 256;
-          float s[64];
-          float mp = -INFINITY;
-          if (w_ok) {
-            tc_fence_after();
-            tmem_ld64(s_tmem + 64 * half, s);
-            if (!full) {
-              const int hi_c = qa - kbase;                           // causal: c <= hi_c
-              const int lo_c = window > 0 ? qa - window + 1 - kbase : -1;
+          for (int c = 0; c < 128; ++c) s[c] = (c <= hi_c && c >= lo_c) ? s[c] : -INFINITY;
+        }
+        float a0 = max3(s[0], s[1], s[2]), a1 = max3(s[3], s[4], s[5]);
+        float a2 = max3(s[6], s[7], s[8]), a3 = max3(s[9], s[10], s[11]);
 #pragma unroll
-              for (int c = 0; c < 64; ++c) s[c] = (c <= hi_c && c >= lo_c) ? s[c] : -INFINITY;
-            }
-            float a0 = max3(s[0], s[1], s[2]), a1 = max3(s[3], s[4], s[5]);
-            float a2 = max3(s[6], s[7], s[8]), a3 = max3(s[9], s[10], s[11]);
+        for (int c = 12; c < 124; c += 8) {
+          a0 = max3(a0, s[c], s[c + 1]);
+          a1 = max3(a1, s[c + 2], s[c + 3]);
+          a2 = max3(a2, s[c + 4], s[c + 5]);
+          a3 = max3(a3, s[c + 6], s[c + 7]);
+        }
+        a0 = max3(a0, s[124], s[125]);
+        a1 = max3(a1, s[126], s[127]);
+        const float mt = fmaxf(max3(a0, a1, a2), a3) * scale_log2;
+        const bool need = mt > m + kRescaleThreshold;  // also true when m == -inf < mt
+        const bool need_o = need && (m != -INFINITY);
+        const float f = need_o ? ex2_mufu(m - mt) : 1.f;   // rescale of the older terms
+        if (need) m = mt;
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        // P = 2^(s * scale_log2 - m) (masked scores are -inf and give 0), its row sum, bf16
+        // P packed two keys per column over the consumed scores: keys 64 hh .. 64 hh + 63 go
+        // to columns 32 hh .. 32 hh + 31
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-mu, -mu);
+        float2 sum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
 #pragma unroll
-            for (int c = 12; c < 60; c += 8) {
-              a0 = max3(a0, s[c], s[c + 1]);
-              a1 = max3(a1, s[c + 2], s[c + 3]);
-              a2 = max3(a2, s[c + 4], s[c + 5]);
-              a3 = max3(a3, s[c + 6], s[c + 7]);
-            }
-            a0 = max3(a0, s[60], s[61]);
-            a1 = max3(a1, s[62], s[63]);
-            mp = fmaxf(max3(a0, a1, a2), a3) * scale_log2;
-            rb[half * 128 + r] = mp;
-          }
-          // both halves have read their scores (P may now overwrite them) and posted maxima
-          if (!bar_and(pair_bar, 64, w_ok)) {
-            ok = false;
-            break;
-          }
-          const float mt = fmaxf(rb[0 * 128 + r], rb[1 * 128 + r]);   // same in both halves
-          const bool need = mt > m[h] + kRescaleThreshold;  // also true when m == -inf < mt
-          const bool need_o = need && (m[h] != -INFINITY);
-          if (__any_sync(0xffffffffu, need_o)) {
-            // O holds P V of tiles < t, all complete: the scores of tile t were issued after
-            const float f = need_o ? ex2_mufu(m[h] - mt) : 1.f;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              float o[32];
-              tmem_ld32(o_tmem + 32 * c, o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= f;
-              tmem_st32(o_tmem + 32 * c, o);
-            }
-            if (need_o) l[h] *= f;
-          }
-          if (need) m[h] = mt;
-          const float mu = (m[h] == -INFINITY) ? 0.f : m[h];
-          // P = 2^(s * scale_log2 - m) (masked scores are -inf and give 0), its row sum, bf16
-          // P packed two keys per column: this half's keys go to columns 32*half .. +31
-          const float2 sc2 = make_float2(scale_log2, scale_log2);
-          const float2 nm2 = make_float2(-mu, -mu);
-          float2 sum[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};
+        for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[32];
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const float2 x = __ffma2_rn(make_float2(s[2 * jj], s[2 * jj + 1]), sc2, nm2);
+            const int c = 64 * hh + 2 * jj;
+            const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), sc2, nm2);
             // two probabilities per MUFU operation, already the bf16 P the P V MMA reads
             const uint32_t p2 = ex2_bf16x2(pack_bf16x2(x.x, x.y));
             pk[jj] = p2;
             sum[jj & 3] = __fadd2_rn(sum[jj & 3], make_float2(__uint_as_float(p2 << 16),
                                                               __uint_as_float(p2 & 0xFFFF0000u)));
           }
-          tmem_st32u(s_tmem + 32 * half, pk);
-          l[h] += ((sum[0].x + sum[0].y) + (sum[1].x + sum[1].y)) +
-                  ((sum[2].x + sum[2].y) + (sum[3].x + sum[3].y));
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(bar(B_PFULL + h));
+          tmem_st32u(s_tmem + 32 * hh, pk);
         }
-      }
+        if (__any_sync(0xffffffffu, need_o)) {
+          // O holds P V of tiles < t, all complete (the scores of tile t were issued after
+          // them); rescaled after P is stored, so that the scores are no longer live
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(o_tmem + 32 * c, o);
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
-        if (h < nh && ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + h), (gt + n - 1) & 1, err));
+            for (int i = 0; i < 32; ++i) o[i] *= f;
+            tmem_st32(o_tmem + 32 * c, o);
+          }
+        }
+        l = l * f + (((sum[0].x + sum[0].y) + (sum[1].x + sum[1].y)) +
+                     ((sum[2].x + sum[2].y) + (sum[3].x + sum[3].y)));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(B_PFULL + wg));
+      }
+      if (active && ok)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE + wg), (gt + n - 1) & 1, err));
       gt += n;
-      // row sums: both halves add the two partial sums in the same order
-      ok = bar_and(pair_bar, 64, ok);    // the partner has read the last maxima
-      if (ok) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (h < nh) red[h * 256 + half * 128 + r] = l[h];
-      }
-      named_barrier_sync(pair_bar, 64);
-      float L[2] = {0.f, 0.f};
-      if (ok) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (h < nh) L[h] = red[h * 256 + r] + red[h * 256 + 128 + r];
-      }
       const bool row_ok = qi < tile.seq_len;
       if (tile.n_chunks == 1) {
-        if (ok) {
+        if (ok && active) {
           tc_fence_after();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          __nv_bfloat16* dst = out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + wg) * 128;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(o_tmem + 32 * c, o);
+            if (row_ok) {
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (h >= nh) break;
-            const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;
-            __nv_bfloat16* dst =
-                out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + h) * 128 + 64 * half;
-            const uint32_t o_tmem = tmem + 256 * h + lane_off + 128 + 64 * half;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              float o[32];
-              tmem_ld32(o_tmem + 32 * c, o);
-              if (row_ok) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                  st_global_v4(dst + 32 * c + i, pack_bf16x2(o[i] * inv, o[i + 1] * inv),
-                               pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
-                               pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
-                               pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
-                }
+              for (int i = 0; i < 32; i += 8) {
+                st_global_v4(dst + 32 * c + i, pack_bf16x2(o[i] * inv, o[i + 1] * inv),
+                             pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv),
+                             pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv),
+                             pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv));
               }
             }
           }
@@ -528,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // but the last stores (max, sum, O) and raises its ready flag, and the last one waits
       // for those flags, then merges in chunk order with its own O still in tensor memory.
       // Partial O of a (slot, head) is [32 dim quads][128 rows][4]: a warp's float4 accesses
-      // at one quad cover 512 contiguous bytes. This half owns quads 16*half .. +15.
+      // at one quad cover 512 contiguous bytes.
       const size_t blk = (size_t)n_q * 128 * 128;    // floats between consecutive slots
       const size_t ml_stride = (size_t)n_q * 128;
       int* const cnt = sc.counters + ((size_t)tile.split * groups + u % groups) * kCounterInts;
@@ -543,15 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       if (order != nc - 1) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h >= nh) break;
-          const size_t hs = (size_t)tile.slot0 * n_q + head0 + h;
-          float* po = sc.part_o + (hs * 128 * 128 + 4 * r) + (size_t)tile.chunk * blk +
-                      (size_t)(16 * half) * 512;
-          const uint32_t o_tmem = tmem + 256 * h + lane_off + 128 + 64 * half;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
+        if (active) {
+          const size_t hs = (size_t)tile.slot0 * n_q + head0 + wg;
+          float* po = sc.part_o + (hs * 128 * 128 + 4 * r) + (size_t)tile.chunk * blk;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
             float o[32];
             tmem_ld32(o_tmem + 32 * c, o);
 #pragma unroll
@@ -559,8 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<float4*>(po + (size_t)((32 * c + i) >> 2) * 512) =
                   make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
           }
-          if (half == 0)
-            sc.part_ml[hs * 128 + r + (size_t)tile.chunk * ml_stride] = make_float2(m[h], L[h]);
+          sc.part_ml[hs * 128 + r + (size_t)tile.chunk * ml_stride] = make_float2(m, l);
         }
         __threadfence();
         named_barrier_sync(1, kSmThreads);
@@ -582,74 +547,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         *merge_flag = ready;
       }
       named_barrier_sync(1, kSmThreads);
-      if (*merge_flag) {
+      const bool merged = *merge_flag != 0;
+      if (merged && active) {
         __threadfence();
         // chunk order, whichever chunk arrives last: M = max m_c, L = sum 2^(m_c - M) l_c,
         // O = sum 2^(m_c - M) O_c, this chunk's terms taken from its registers and TMEM
+        const size_t hs = (size_t)tile.slot0 * n_q + head0 + wg;
+        const float2* ml0 = sc.part_ml + hs * 128 + r;
+        const float* po0 = sc.part_o + (hs * 128 * 128 + 4 * r);
+        float f[kMaxChunks], lc[kMaxChunks];
+        float M = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h >= nh) break;
-          const size_t hs = (size_t)tile.slot0 * n_q + head0 + h;
-          const float2* ml0 = sc.part_ml + hs * 128 + r;
-          const float* po0 = sc.part_o + (hs * 128 * 128 + 4 * r) + (size_t)(16 * half) * 512;
-          float f[kMaxChunks], lc[kMaxChunks];
-          float M = -INFINITY;
+        for (int c = 0; c < kMaxChunks; ++c) {
+          float2 v = make_float2(-INFINITY, 0.f);
+          if (c == tile.chunk) v = make_float2(m, l);
+          else if (c < nc) v = ld_cg_f2(ml0 + c * ml_stride);
+          f[c] = v.x;
+          lc[c] = v.y;
+          M = fmaxf(M, v.x);
+        }
+        float Lm = 0.f;
 #pragma unroll
-          for (int c = 0; c < kMaxChunks; ++c) {
-            float2 v = make_float2(-INFINITY, 0.f);
-            if (c == tile.chunk) v = make_float2(m[h], L[h]);
-            else if (c < nc) v = ld_cg_f2(ml0 + c * ml_stride);
-            f[c] = v.x;
-            lc[c] = v.y;
-            M = fmaxf(M, v.x);
-          }
-          float Lm = 0.f;
-#pragma unroll
-          for (int c = 0; c < kMaxChunks; ++c) {
-            f[c] = (f[c] == -INFINITY) ? 0.f : ex2_mufu(f[c] - M);
-            Lm += f[c] * lc[c];
-          }
-          const float inv = Lm > 0.f ? 1.f / Lm : 0.f;
-          __nv_bfloat16* dst =
-              out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + h) * 128 + 64 * half;
-          const uint32_t o_tmem = tmem + 256 * h + lane_off + 128 + 64 * half;
+        for (int c = 0; c < kMaxChunks; ++c) {
+          f[c] = (f[c] == -INFINITY) ? 0.f : ex2_mufu(f[c] - M);
+          Lm += f[c] * lc[c];
+        }
+        const float inv = Lm > 0.f ? 1.f / Lm : 0.f;
+        __nv_bfloat16* dst = out + (size_t)(tile.seq_start + qi) * ld_out + (head0 + wg) * 128;
 #pragma unroll 1
-          for (int cb = 0; cb < 4; ++cb) {   // 16 dims per pass
-            float own[16];
-            tmem_ld16(o_tmem + 16 * cb, own);
-            float acc[16];
+        for (int cb = 0; cb < 8; ++cb) {   // 16 dims per pass
+          float own[16];
+          tmem_ld16(o_tmem + 16 * cb, own);
+          float acc[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+          for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < nc; ++c) {
-              if (c == tile.chunk) {
+          for (int c = 0; c < nc; ++c) {
+            if (c == tile.chunk) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] += f[c] * own[i];
-              } else {
-                const float* po = po0 + (size_t)c * blk + (size_t)(4 * cb) * 512;
+              for (int i = 0; i < 16; ++i) acc[i] += f[c] * own[i];
+            } else {
+              const float* po = po0 + (size_t)c * blk + (size_t)(4 * cb) * 512;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const float4 v = ld_cg_f4(po + k * 512);
-                  acc[4 * k] += f[c] * v.x;
-                  acc[4 * k + 1] += f[c] * v.y;
-                  acc[4 * k + 2] += f[c] * v.z;
-                  acc[4 * k + 3] += f[c] * v.w;
-                }
+              for (int k = 0; k < 4; ++k) {
+                const float4 v = ld_cg_f4(po + k * 512);
+                acc[4 * k] += f[c] * v.x;
+                acc[4 * k + 1] += f[c] * v.y;
+                acc[4 * k + 2] += f[c] * v.z;
+                acc[4 * k + 3] += f[c] * v.w;
               }
             }
-            if (row_ok) {
+          }
+          if (row_ok) {
 #pragma unroll
-              for (int i = 0; i < 16; i += 8) {
-                st_global_v4(dst + 16 * cb + i, pack_bf16x2(acc[i] * inv, acc[i + 1] * inv),
-                             pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv),
-                             pack_bf16x2(acc[i + 4] * inv, acc[i + 5] * inv),
-                             pack_bf16x2(acc[i + 6] * inv, acc[i + 7] * inv));
-              }
+            for (int i = 0; i < 16; i += 8) {
+              st_global_v4(dst + 16 * cb + i, pack_bf16x2(acc[i] * inv, acc[i + 1] * inv),
+                           pack_bf16x2(acc[i + 2] * inv, acc[i + 3] * inv),
+                           pack_bf16x2(acc[i + 4] * inv, acc[i + 5] * inv),
+                           pack_bf16x2(acc[i + 6] * inv, acc[i + 7] * inv));
             }
           }
         }
       }
-      ok = bar_and(1, kSmThreads, ok && *merge_flag);
+      ok = bar_and(1, kSmThreads, ok && merged);
     }
   }
   __syncthreads();
