@@ -18,6 +18,7 @@ from cohere_compass_decoder_gb300.model import to_device
 import cohere_compass_decoder_gb300._lib as L
 
 from gpu_util import require_gpu, assert_close, err_stats
+from conftest import read_golden
 
 pytestmark = pytest.mark.gpu
 
@@ -135,6 +136,16 @@ def test_a_device_wait_that_runs_out_reports_timeout_and_the_plan_recovers():
     gw.sync()
     _check(inp, gw, h2, lg2)
     gw.close()
+
+
+def test_small_stack_single_row_block_splits_the_output_projection():
+    """T = 100 (one row block): the output projection splits K, adds with reductions, and its
+    last split per column tile normalises the updated rows for the next layer."""
+    inp = _small("small_rb1", [100], [ImageSpan(0, 20, 1, 4, 6)], 2,
+                 types=(SLIDING, FULL, SLIDING), hidden=2048, inter=1024, heads=(16, 4),
+                 vocab=256, seed=34)
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
 
 
 def test_small_stack_mha_and_no_images():
@@ -534,17 +545,38 @@ def test_stack28_every_layer_from_oracle_input(stack28_oracle):
 
 @pytest.mark.slow
 def test_stack28_T8192(stack28_oracle):
-    """The whole 28-layer stack and the head, end to end. Two bf16 implementations that
-    round the same intermediates drift apart by independent rounding noise once any
-    residual differs by an ulp; the oracle's own bf16-mirror mode drifts from its exact fp64
-    mode by 0.040 mean-abs / 0.24 max-abs after these 28 layers (per-layer growth about
-    1.4e-3). The end-to-end bound is therefore 1.5x that floor: 0.06 mean-abs, 0.5 max-abs
-    on the final hidden state; the logits keep the stack tolerance."""
+    """The whole 28-layer stack and the head, end to end, within a bound derived from the
+    oracle alone (tests/golden/stack28_T8192_mirror_drift.txt, written by
+    tests/golden/make_stack28_drift.py). Moving every input element by one float32 ulp (the
+    resolution of the GPU's fp32 residual stream) flips some of the bf16 roundings the
+    contract prescribes, and the oracle's own mirror result then drifts by a mean-abs that grows
+    about linearly with depth, to the recorded floor after 28 layers; the GPU, whose fp32
+    accumulation differs from the oracle's fp64 at every layer, sits on the same growth. Bound:
+    1.25x the floor on the mean-abs and 1.5x on the max-abs (an extreme value over 16.8 M
+    elements) of the final hidden state; the logits keep the benchmark spec's bound (2e-2 max-abs,
+    2e-3 mean-abs) and 2% of their largest magnitude, twice the floor's 1%."""
+    g = read_golden("stack28_T8192_mirror_drift.txt")
     inp, hs, lg_ref = stack28_oracle
     gw, h, lg = _run(inp)
-    assert_close(as_numpy(h), hs[-1], 0.5, 0.06, "hidden after 28 layers")
+    mx, mn = assert_close(as_numpy(h), hs[-1], 1.5 * g["fp32_ulp_hidden_max"][0],
+                          1.25 * g["fp32_ulp_hidden_mean"][0], "hidden after 28 layers")
     lmx, _ = assert_close(as_numpy(lg), lg_ref, TOL_MAX, TOL_MEAN, "logits")
-    assert lmx / np.abs(lg_ref).max() <= 0.1
+    rel = lmx / np.abs(lg_ref).max()
+    print(f"hidden max {mx:.4g} mean {mn:.4g} (floor {g['fp32_ulp_hidden_max'][0]:.4g} / "
+          f"{g['fp32_ulp_hidden_mean'][0]:.4g}); logits rel {rel:.4g}")
+    assert rel <= 2e-2, f"logits relative error {rel:.3g}"
+
+
+def test_pair_shapes_with_a_ragged_row_block_past_one_round():
+    """The two-layer pair's shapes at T = 2610: 21 row blocks of 128 x 256 output tiles (the
+    last one ragged) in the output projection with the fused next-layer LayerNorm, more row
+    blocks than one round of tiles holds."""
+    from synth.configs import SHAPE_PAIR
+    inp = Inputs(Workload("pair_T2610", SHAPE_PAIR, "prefill", [2610],
+                          images=[ImageSpan(0, 2300, 1, 12, 16)], n_deepstack=1,
+                          head_rows="last", seed=33))
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
 
 
 @pytest.mark.slow

@@ -577,3 +577,26 @@ def test_dequantize_affine_worked_example():
     # the descending half of group 0: q = 15 - (k - 16)
     assert w[0, 16:32].tolist() == [0.5 * (15 - i) - 2.0 for i in range(16)]
     assert np.all(w[0, 48:64] == 0.5 * 7 - 2.0)
+
+
+def test_drift_script_moves_each_element_by_one_unit_in_the_last_place():
+    """The perturbation behind the 28-layer end-to-end bound (tests/golden/
+    make_stack28_drift.py) moves every element by exactly one float32 (or bf16) ulp."""
+    import importlib.util, os
+    from conftest import GOLDEN
+    spec = importlib.util.spec_from_file_location("make_drift",
+                                                  os.path.join(GOLDEN, "make_stack28_drift.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    x = np.random.default_rng(3).standard_normal(5000).astype(np.float32).astype(np.float64)
+    y = mod.nudge(x, 23, 1)
+    up = np.nextafter(x.astype(np.float32), np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(x.astype(np.float32), np.float32(-np.inf)).astype(np.float64)
+    # one ulp of the binade of x (at a power of two, the step down is half as large: still one
+    # unit in the last place of x's own binade)
+    ok = (y == up) | (y == dn) | (np.abs(y - x) == np.abs(up - x))
+    assert ok.all()
+    xb = O.round_bf16(x)
+    yb = mod.nudge(xb, 7, 2)
+    assert np.array_equal(O.round_bf16(yb), yb)            # still a bf16 value
+    assert (np.abs(yb - xb) == np.exp2(np.floor(np.log2(np.abs(xb))) - 7)).all()
