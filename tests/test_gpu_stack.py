@@ -139,8 +139,8 @@ def test_a_device_wait_that_runs_out_reports_timeout_and_the_plan_recovers():
 
 
 def test_small_stack_single_row_block_splits_the_output_projection():
-    """T = 100 (one row block): the output projection splits K, adds with reductions, and its
-    last split per column tile normalises the updated rows for the next layer."""
+    """T = 100 (one row block) at the pair's hidden size: the output projection splits K and
+    adds with reductions, and each layer's LayerNorm runs as its own kernel."""
     inp = _small("small_rb1", [100], [ImageSpan(0, 20, 1, 4, 6)], 2,
                  types=(SLIDING, FULL, SLIDING), hidden=2048, inter=1024, heads=(16, 4),
                  vocab=256, seed=34)
