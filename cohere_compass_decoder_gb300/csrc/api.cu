@@ -506,7 +506,8 @@ static cc_status plan_gemm(const CUtensorMap& ta, const CUtensorMap& b128, const
                            cudaStream_t s) {
   int bn, splits;
   gemm_choose(M, N, K, epi, &bn, &splits);
-  return launch_gemm(ta, bn == 256 ? b256 : b128, M, N, K, bn, splits, epi, ep, err, s);
+  return launch_gemm(ta, bn == 256 ? b256 : b128, M, N, K, bn, splits, epi, ep, err, s,
+                     bn == 256 ? &b128 : nullptr);
 }
 
 // Token-id input of the prefill: the embedding merge fused with layer 0's LayerNorm.

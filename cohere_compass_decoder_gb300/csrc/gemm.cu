@@ -39,6 +39,7 @@ struct GemmCfg {
 
 struct Unit {
   int mt, nt, kb0, kb1;
+  int n0, nw;   // first output column and width (decode_item)
 };
 
 // Unit u of a launch. m fastest (the default): CTAs running together share the weight tile.
@@ -59,6 +60,31 @@ __device__ __forceinline__ Unit decode_unit(int u, int m_tiles, int n_tiles, int
   }
   r.kb0 = (kbt * sp) / splits;
   r.kb1 = (kbt * (sp + 1)) / splits;
+  return r;
+}
+
+// Work item i of a k_gemm launch. Items before `tail0` are the units of decode_unit, BN
+// columns wide. From `tail0` on (only the residual + LayerNorm launch, and only when its last
+// round of units would be at most half full) every remaining BN-wide tile is two items of BN/2
+// columns with the whole K loop, taken by distinct CTAs, so that the last round costs half a
+// tile. tail0 is a whole number of row blocks; the halves of a row block are consecutive.
+template <int BN>
+__device__ __forceinline__ Unit decode_item(int i, int m_tiles, int n_tiles, int splits, int kbt,
+                                            bool n_fast, int tail0) {
+  Unit r;
+  if (i < tail0) {
+    r = decode_unit(i, m_tiles, n_tiles, splits, kbt, n_fast);
+    r.n0 = r.nt * BN;
+    r.nw = BN;
+  } else {
+    const int j = i - tail0, per_block = 2 * n_tiles;
+    r.mt = tail0 / n_tiles + j / per_block;
+    r.nt = -1;
+    r.n0 = (j % per_block) * (BN / 2);
+    r.nw = BN / 2;
+    r.kb0 = 0;
+    r.kb1 = kbt;
+  }
   return r;
 }
 
@@ -254,34 +280,49 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int row, int n0, i
   }
 }
 
+// Loads 32 consecutive fp32 values (128 bytes) of one row.
+__device__ __forceinline__ void ld_f32x32(const float* src, float4* v) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = s4[i];
+}
+
 // EPI_RESID_LN: the residual update of EPI_RESID followed by the next layer's LayerNorm of
 // the updated rows (mlxcel issue "Cohere Compass / North-Micro-Vision", "Text decoder
 // forward": a = LayerNorm(h), weight only, biased variance, eps inside the root, statistics
-// in f32). Pass 1 stores h += acc (+ deepstack) and this tile's (mean, M2) of the row over
-// its BN columns (Chan's update per 32-column chunk); the tile counts itself in its row
-// block's counter and waits (bounded) for the block's other N / BN tiles, which run at the
-// same time on other CTAs. Pass 2 merges the partials of the row (equal counts: mean = the
-// average of the means, M2 = sum M2_i + BN sum (mean_i - mean)^2), re-reads this tile's
-// columns of h and stores bf16((h - mean) * rstd * gamma). Returns false when the wait gave
-// up (every epilogue thread gets the same answer).
+// in f32). The tile covers columns [n0, n0 + nw) of its row block, nw = BN or BN / 2 (a tail
+// half). Pass 1 stores h += acc (+ deepstack), keeps the updated h in the tile's own TMEM
+// columns (the accumulator is not released before pass 2 ends) and, per 128-column slot of
+// the row, stores the slot's (mean, M2) (Chan's update per 32-column chunk); the residual of
+// the next chunk is loaded while the current one is processed. The tile adds its slot count
+// to the row block's counter and waits (bounded) for the block's other tiles, which run at
+// the same time on other CTAs, until all N / 128 slots are in. Pass 2 merges the slots (equal
+// counts: mean = the average of the means, M2 = sum M2_i + 128 sum (mean_i - mean)^2) and
+// stores bf16((h - mean) * rstd * gamma) from the h held in TMEM. Returns false when the wait
+// gave up (every epilogue thread gets the same answer).
 template <int BN>
-__device__ __forceinline__ bool epilogue_resid_ln(uint32_t t_row, int row, int mt, int nt,
-                                                  int n_tiles, int M, const EpiParams& ep,
+__device__ __forceinline__ bool epilogue_resid_ln(uint32_t t_row, int row, int mt, int n0, int nw,
+                                                  int n_slots, int M, const EpiParams& ep,
                                                   int* err, volatile int* flag) {
   const bool row_ok = row < M;
-  const int n0 = nt * BN;
   const __nv_bfloat16* ds_row = nullptr;
   if (ep.ds_map && row_ok) {
     const int r = ep.ds_map[row];
     if (r >= 0) ds_row = ep.ds + (size_t)r * ep.ldc;
   }
   float* hrow = ep.c + (size_t)row * ep.ldc + n0;
+  float2* slots = ep.ln_part + (size_t)row * n_slots + (n0 >> 7);
   float mean = 0.f, m2 = 0.f;
+  float4 hn[8];
+  if (row_ok) ld_f32x32(hrow, hn);
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
+  for (int c = 0; c < nw; c += 32) {
+    float4 hc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hc[i] = hn[i];
+    if (row_ok && c + 32 < nw) ld_f32x32(hrow + c + 32, hn);
     float v[32];
     tmem_ld32(t_row + c, v);
-    if (!row_ok) continue;
     if (ds_row) {
 #pragma unroll
       for (int i = 0; i < 32; i += 2) {
@@ -290,16 +331,19 @@ __device__ __forceinline__ bool epilogue_resid_ln(uint32_t t_row, int row, int m
         v[i + 1] += __bfloat162float(d2.y);
       }
     }
-    float4* d4 = reinterpret_cast<float4*>(hrow + c);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float4 p = d4[i];
-      v[4 * i] += p.x;
-      v[4 * i + 1] += p.y;
-      v[4 * i + 2] += p.z;
-      v[4 * i + 3] += p.w;
-      d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      v[4 * i] += hc[i].x;
+      v[4 * i + 1] += hc[i].y;
+      v[4 * i + 2] += hc[i].z;
+      v[4 * i + 3] += hc[i].w;
     }
+    tmem_st32(t_row + c, v);
+    if (!row_ok) continue;
+    float4* d4 = reinterpret_cast<float4*>(hrow + c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     float sum = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) sum += v[i];
@@ -310,51 +354,61 @@ __device__ __forceinline__ bool epilogue_resid_ln(uint32_t t_row, int row, int m
       const float d = v[i] - mc;
       q += d * d;
     }
-    const float na = static_cast<float>(c), tot = na + 32.0f;
+    const float na = static_cast<float>(c & 127), tot = na + 32.0f;
     const float delta = mc - mean;
     mean += delta * (32.0f / tot);
     m2 += q + delta * delta * (na * 32.0f / tot);
+    if ((c & 127) == 96) {   // the slot's 128 columns are in
+      slots[c >> 7] = make_float2(mean, m2);
+      mean = 0.f;
+      m2 = 0.f;
+    }
   }
-  if (row_ok) ep.ln_part[(size_t)row * n_tiles + nt] = make_float2(mean, m2);
+  tmem_st_wait();
   __threadfence();
   epi_bar();
-  if (threadIdx.x == 64) {   // the first epilogue thread counts the tile and waits
+  if (threadIdx.x == 64) {   // the first epilogue thread counts the tile's slots and waits
     int32_t* cnt = ep.ln_cnt + mt;
-    atomicAdd(cnt, 1);
-    *flag = wait_count(cnt, n_tiles, err) ? 1 : 0;
+    atomicAdd(cnt, nw >> 7);
+    *flag = wait_count(cnt, n_slots, err) ? 1 : 0;
   }
   epi_bar();
   if (*flag == 0) return false;
+  float mu = 0.f, rstd = 0.f;
   if (row_ok) {
-    const float2* part = ep.ln_part + (size_t)row * n_tiles;
+    const float2* part = ep.ln_part + (size_t)row * n_slots;
     float sm = 0.f;
 #pragma unroll 1
-    for (int i = 0; i < n_tiles; ++i) sm += ld_cg_f2(part + i).x;
-    const float mu = sm / static_cast<float>(n_tiles);
+    for (int i = 0; i < n_slots; ++i) sm += ld_cg_f2(part + i).x;
+    mu = sm / static_cast<float>(n_slots);
     float q = 0.f;
 #pragma unroll 1
-    for (int i = 0; i < n_tiles; ++i) {
+    for (int i = 0; i < n_slots; ++i) {
       const float2 pm = ld_cg_f2(part + i);
       const float d = pm.x - mu;
-      q += pm.y + static_cast<float>(BN) * d * d;
+      q += pm.y + 128.0f * d * d;
     }
-    const float rstd = rsqrtf(q / static_cast<float>(n_tiles * BN) + ep.ln_eps);
-    __nv_bfloat16* dst = ep.ln_out + (size_t)row * ep.ldc + n0;
-    const __nv_bfloat16* gam = ep.ln_gamma + n0;
-#pragma unroll 4
-    for (int c = 0; c < BN; c += 8) {
-      const float4 x0 = *reinterpret_cast<const float4*>(hrow + c);
-      const float4 x1 = *reinterpret_cast<const float4*>(hrow + c + 4);
-      const uint4 graw = __ldg(reinterpret_cast<const uint4*>(gam + c));
+    rstd = rsqrtf(q / static_cast<float>(n_slots * 128) + ep.ln_eps);
+  }
+  __nv_bfloat16* dst = ep.ln_out + (size_t)row * ep.ldc + n0;
+  const __nv_bfloat16* gam = ep.ln_gamma + n0;
+#pragma unroll 1
+  for (int c = 0; c < nw; c += 32) {
+    float x[32];
+    tmem_ld32(t_row + c, x);
+    if (!row_ok) continue;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      const uint4 graw = __ldg(reinterpret_cast<const uint4*>(gam + c + i));
       const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
       const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
       const float2 g2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.z));
       const float2 g3 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.w));
-      *reinterpret_cast<uint4*>(dst + c) = make_uint4(
-          pack_bf16x2((x0.x - mu) * rstd * g0.x, (x0.y - mu) * rstd * g0.y),
-          pack_bf16x2((x0.z - mu) * rstd * g1.x, (x0.w - mu) * rstd * g1.y),
-          pack_bf16x2((x1.x - mu) * rstd * g2.x, (x1.y - mu) * rstd * g2.y),
-          pack_bf16x2((x1.z - mu) * rstd * g3.x, (x1.w - mu) * rstd * g3.y));
+      st_global_v4(dst + c + i,
+                   pack_bf16x2((x[i] - mu) * rstd * g0.x, (x[i + 1] - mu) * rstd * g0.y),
+                   pack_bf16x2((x[i + 2] - mu) * rstd * g1.x, (x[i + 3] - mu) * rstd * g1.y),
+                   pack_bf16x2((x[i + 4] - mu) * rstd * g2.x, (x[i + 5] - mu) * rstd * g2.y),
+                   pack_bf16x2((x[i + 6] - mu) * rstd * g3.x, (x[i + 7] - mu) * rstd * g3.y));
     }
   }
   return true;
@@ -363,7 +417,8 @@ __device__ __forceinline__ bool epilogue_resid_ln(uint32_t t_row, int row, int m
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-           int M, int N, int K, int splits, const EpiParams ep, int* err) {
+           const __grid_constant__ CUtensorMap tm_b_half, int M, int N, int K, int splits,
+           int tail0, const EpiParams ep, int* err) {
   using C = GemmCfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -382,6 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t never = smem_u32(bars + 2 * S + 7);   // test hook: nothing arrives on it
   volatile int* ln_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 8);
   constexpr bool kNFast = EPI == EPI_RESID_LN;
+  // tail halves (decode_item) only in the 256-wide residual + LayerNorm launch
+  constexpr bool kHalves = EPI == EPI_RESID_LN && BN == 256;
 
   pdl_trigger();
   const int warp = warp_id(), lane = lane_id();
@@ -389,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = N / BN;
   const int kbt = K / kBK;
   const int units = m_tiles * n_tiles * splits;
+  if (!kHalves) tail0 = units;
+  const int items = tail0 + 2 * (units - tail0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -411,6 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
+    if (kHalves && tail0 < units) tma_prefetch_desc(&tm_b_half);
   }
   tc_fence_before();
   __syncthreads();
@@ -424,17 +484,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt, kNFast);
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+        const Unit t = decode_item<BN>(u, m_tiles, n_tiles, splits, kbt, kNFast, tail0);
+        const bool half = kHalves && t.nw != BN;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, err)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * stage;
-          mbar_expect_tx(fb, C::kStageBytes);
+          mbar_expect_tx(fb, half ? C::kABytes + C::kBBytes / 2 : C::kStageBytes);
           tma_load_2d(smem_u32(sA + stage * C::kABytes), &tm_a, fb, kb * kBK, t.mt * kBM);
-          tma_load_2d(smem_u32(sB + stage * C::kBBytes), &tm_b, fb, kb * kBK, t.nt * BN);
+          tma_load_2d(smem_u32(sB + stage * C::kBBytes), half ? &tm_b_half : &tm_b, fb, kb * kBK,
+                      t.n0);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -446,13 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, 0);
+      constexpr uint32_t kIdescHalf = idesc_bf16(kBM, BN / 2, 0);
       int stage = 0;
       uint32_t phase = 0;
       int iter = 0, consumed = 0;
       bool ok = true;
       if (ep.test_stall) ok = mbar_wait(never, 0, err, kTestStallCycles);
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++iter) {
-        const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt, kNFast);
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x, ++iter) {
+        const Unit t = decode_item<BN>(u, m_tiles, n_tiles, splits, kbt, kNFast, tail0);
+        const uint32_t idesc = (kHalves && t.nw != BN) ? kIdescHalf : kIdesc;
         const int acc = iter & 1;
         if (!mbar_wait(tempty0 + 8 * acc, ((iter >> 1) & 1) ^ 1, err)) {
           ok = false;
@@ -471,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            tc_mma(d_tmem, desc_kmajor_sw128(a0 + 32 * k), desc_kmajor_sw128(b0 + 32 * k), kIdesc,
+            tc_mma(d_tmem, desc_kmajor_sw128(a0 + 32 * k), desc_kmajor_sw128(b0 + 32 * k), idesc,
                    (kb > t.kb0 || k > 0) ? 1u : 0u);
           }
           tc_commit(empty0 + 8 * stage);
@@ -491,17 +555,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     int iter = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++iter) {
-      const Unit t = decode_unit(u, m_tiles, n_tiles, splits, kbt, kNFast);
+    for (int u = blockIdx.x; u < items; u += gridDim.x, ++iter) {
+      const Unit t = decode_item<BN>(u, m_tiles, n_tiles, splits, kbt, kNFast, tail0);
       const int acc = iter & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (iter >> 1) & 1, err))) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + acc * BN + (static_cast<uint32_t>(quarter * 32) << 16);
       const int row = t.mt * kBM + quarter * 32 + lane;
       if constexpr (EPI == EPI_RESID_LN) {
-        if (!epilogue_resid_ln<BN>(t_row, row, t.mt, t.nt, n_tiles, M, ep, err, ln_flag)) break;
+        if (!epilogue_resid_ln<BN>(t_row, row, t.mt, t.n0, t.nw, N >> 7, M, ep, err, ln_flag))
+          break;
       } else {
-        epilogue_tile<BN, EPI>(t_row, row, t.nt * BN, M, t.kb0, splits, ep);
+        epilogue_tile<BN, EPI>(t_row, row, t.n0, M, t.kb0, splits, ep);
       }
       tc_fence_before();
       mbar_arrive(tempty0 + 8 * acc);
@@ -521,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN, int EPI>
-cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int splits,
-                   const EpiParams& ep, int* err, cudaStream_t s) {
+cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tb_half, int M,
+                   int N, int K, int splits, const EpiParams& ep, int* err, cudaStream_t s) {
   using C = GemmCfg<BN>;
   static std::atomic<bool> smem_set{false};
   auto kern = k_gemm<BN, EPI>;
@@ -530,15 +595,19 @@ cc_status launch_t(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, i
   const int m_tiles = (M + kBM - 1) / kBM;
   const int units = m_tiles * (N / BN) * splits;
   int grid = units < num_sms() ? units : num_sms();
+  int tail0 = units;
   if (EPI == EPI_RESID_LN) {
     // the N / BN tiles of a row block are consecutive units: with the grid a multiple of
     // N / BN they run in the same round, each on its own CTA (one resident CTA per SM)
     const int nt = N / BN;
     if (nt > num_sms() || splits != 1) return CC_ERR_UNSUPPORTED;
     grid = std::min(units, (num_sms() / nt) * nt);
+    // a last round at most half full runs as 128-column halves of its tiles (decode_item)
+    const int rounds = units / grid, rem = units - rounds * grid;
+    if (BN == 256 && tb_half && rem > 0 && 2 * rem <= grid) tail0 = rounds * grid;
   }
-  CC_CHECK_CUDA(launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmem, s, ta, tb, M, N, K, splits,
-                          ep, err));
+  CC_CHECK_CUDA(launch_pdl(kern, dim3(grid), dim3(kThreads), C::kSmem, s, ta, tb,
+                          tb_half ? *tb_half : tb, M, N, K, splits, tail0, ep, err));
   return CC_OK;
 }
 
@@ -1034,7 +1103,8 @@ static std::atomic<int> g_test_stall_next{0};
 void test_stall_next_gemm() { g_test_stall_next.store(1); }
 
 cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int bn,
-                      int splits, int epi, const EpiParams& ep_in, int* err, cudaStream_t s) {
+                      int splits, int epi, const EpiParams& ep_in, int* err, cudaStream_t s,
+                      const CUtensorMap* tb_half) {
   if (M <= 0) return CC_OK;
   if (K % kBK != 0 || N % bn != 0 || splits < 1 || splits > K / kBK)
     return CC_ERR_INVALID_ARG;
@@ -1043,17 +1113,25 @@ cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N
     ep.test_stall = 1;
   if (bn == 256) {
     switch (epi) {
-      case EPI_F32: return launch_t<256, EPI_F32>(ta, tb, M, N, K, splits, ep, err, s);
-      case EPI_RESID: return launch_t<256, EPI_RESID>(ta, tb, M, N, K, splits, ep, err, s);
-      case EPI_QKV_MLP: return launch_t<256, EPI_QKV_MLP>(ta, tb, M, N, K, 1, ep, err, s);
-      case EPI_RESID_LN: return launch_t<256, EPI_RESID_LN>(ta, tb, M, N, K, splits, ep, err, s);
+      case EPI_F32:
+        return launch_t<256, EPI_F32>(ta, tb, tb_half, M, N, K, splits, ep, err, s);
+      case EPI_RESID:
+        return launch_t<256, EPI_RESID>(ta, tb, tb_half, M, N, K, splits, ep, err, s);
+      case EPI_QKV_MLP:
+        return launch_t<256, EPI_QKV_MLP>(ta, tb, tb_half, M, N, K, 1, ep, err, s);
+      case EPI_RESID_LN:
+        return launch_t<256, EPI_RESID_LN>(ta, tb, tb_half, M, N, K, splits, ep, err, s);
     }
   } else if (bn == 128) {
     switch (epi) {
-      case EPI_F32: return launch_t<128, EPI_F32>(ta, tb, M, N, K, splits, ep, err, s);
-      case EPI_RESID: return launch_t<128, EPI_RESID>(ta, tb, M, N, K, splits, ep, err, s);
-      case EPI_QKV_MLP: return launch_t<128, EPI_QKV_MLP>(ta, tb, M, N, K, 1, ep, err, s);
-      case EPI_RESID_LN: return launch_t<128, EPI_RESID_LN>(ta, tb, M, N, K, splits, ep, err, s);
+      case EPI_F32:
+        return launch_t<128, EPI_F32>(ta, tb, tb_half, M, N, K, splits, ep, err, s);
+      case EPI_RESID:
+        return launch_t<128, EPI_RESID>(ta, tb, tb_half, M, N, K, splits, ep, err, s);
+      case EPI_QKV_MLP:
+        return launch_t<128, EPI_QKV_MLP>(ta, tb, tb_half, M, N, K, 1, ep, err, s);
+      case EPI_RESID_LN:
+        return launch_t<128, EPI_RESID_LN>(ta, tb, tb_half, M, N, K, splits, ep, err, s);
     }
   }
   return CC_ERR_INVALID_ARG;

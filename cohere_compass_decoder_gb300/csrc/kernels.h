@@ -43,9 +43,9 @@ struct EpiParams {
   __nv_bfloat16* act_out = nullptr;      // [M, ld_act]
   int ld_act = 0;
   // EPI_RESID_LN: ln_out[row] = bf16(LayerNorm(h[row]) * ln_gamma) of the updated rows. Each
-  // output tile stores its rows' (mean, M2) over its columns in ln_part [M, N / BN] and counts
-  // itself in ln_cnt[m-tile] (zero when the launch starts; left at N / BN); the tiles of a
-  // row block meet there and each normalises its own columns.
+  // output tile stores its rows' (mean, M2) per 128-column slot in ln_part [M, N / 128] and
+  // adds its slot count to ln_cnt[m-tile] (zero when the launch starts; left at N / 128); the
+  // tiles of a row block meet there and each normalises its own columns.
   const __nv_bfloat16* ln_gamma = nullptr;
   __nv_bfloat16* ln_out = nullptr;       // [M, ldc]
   float2* ln_part = nullptr;
@@ -59,8 +59,11 @@ struct EpiParams {
 // C[M,N] (epilogue) = A[M,K] @ B[N,K]^T with A, B given by TMA maps (bf16, box 64 x 128
 // for A and 64 x BN for B, 128-byte swizzle). bn is 128 or 256; splits divides the
 // K loop (splits > 1 needs an additive epilogue: EPI_RESID or EPI_F32 with accumulate).
+// tb_half (optional): the same weights with a 128-row box; with it a 256-wide EPI_RESID_LN
+// launch runs a last round that is at most half full as 128-column halves of its tiles.
 cc_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, int bn,
-                      int splits, int epi, const EpiParams& ep, int* err, cudaStream_t s);
+                      int splits, int epi, const EpiParams& ep, int* err, cudaStream_t s,
+                      const CUtensorMap* tb_half = nullptr);
 
 // Test hook: the next launch_gemm call (any thread) stalls its MMA thread (EpiParams::test_stall).
 void test_stall_next_gemm();

@@ -570,7 +570,8 @@ def test_stack28_T8192(stack28_oracle):
 def test_pair_shapes_with_a_ragged_row_block_past_one_round():
     """The two-layer pair's shapes at T = 2610: 21 row blocks of 128 x 256 output tiles (the
     last one ragged) in the output projection with the fused next-layer LayerNorm, more row
-    blocks than one round of tiles holds."""
+    blocks than one round of tiles holds. The two row blocks past the first round (the ragged
+    one, and image rows that take the deepstack add) run as 128-column tile halves."""
     from synth.configs import SHAPE_PAIR
     inp = Inputs(Workload("pair_T2610", SHAPE_PAIR, "prefill", [2610],
                           images=[ImageSpan(0, 2300, 1, 12, 16)], n_deepstack=1,
