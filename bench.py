@@ -295,6 +295,7 @@ def prefill_leg(args, dist, pk, key, context=False):
     if g1:
         g1["tflops"] = ach
         g1["frac_of_bf16_peak"] = ach / pk["bf16"]
+        g1["frac_of_sustained"] = ach / pk["bf16_sus"]
     # other classes against their own roofs
     g2 = kern.get("gemm_out_resid")
     if g2:
@@ -302,11 +303,13 @@ def prefill_leg(args, dist, pk, key, context=False):
         f2 = 2.0 * T * s.hidden_size * K2
         g2["tflops"] = f2 / (g2["avg_us"] * 1e-6) / 1e12
         g2["frac_of_bf16_peak"] = g2["tflops"] / pk["bf16"]
+        g2["frac_of_sustained"] = g2["tflops"] / pk["bf16_sus"]
     at = kern.get("attn_prefill")
     if at:
         fa = attn_flops(inp) / at["launches_per_step"]
         at["tflops"] = fa / (at["avg_us"] * 1e-6) / 1e12
         at["frac_of_bf16_peak"] = at["tflops"] / pk["bf16"]
+        at["frac_of_sustained"] = at["tflops"] / pk["bf16_sus"]
     gh = kern.get("gemm_head")
     if gh:
         hb = s.vocab_size * s.hidden_size * 2 + len(inp.head_rows) * s.vocab_size * 4
