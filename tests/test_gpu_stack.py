@@ -580,6 +580,20 @@ def test_pair_shapes_with_a_ragged_row_block_past_one_round():
     _check(inp, gw, h, lg)
 
 
+def test_pair_shapes_with_a_last_round_more_than_half_full():
+    """The two-layer pair's shapes at T = 3700: 29 row blocks (the last one ragged), 232 output
+    tiles of 128 x 256 in the output projection with the fused next-layer LayerNorm. The
+    second round holds 80 tiles on 152 CTAs, more than half, so it runs as whole tiles (as
+    halves it would take two rounds of 128-column tiles); image rows there take the deepstack
+    add."""
+    from synth.configs import SHAPE_PAIR
+    inp = Inputs(Workload("pair_T3700", SHAPE_PAIR, "prefill", [3700],
+                          images=[ImageSpan(0, 3000, 1, 12, 16)], n_deepstack=1,
+                          head_rows="last", seed=34))
+    gw, h, lg = _run(inp)
+    _check(inp, gw, h, lg)
+
+
 @pytest.mark.slow
 def test_varlen_T32768():
     inp = Inputs(varlen_T32768())
