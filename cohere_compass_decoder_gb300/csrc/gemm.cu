@@ -15,6 +15,8 @@
 //                stored bf16 (k, v also into the paged cache), SwiGLU silu(g) * u -> bf16
 //   EPI_RESID    h += o_proj(attn) + down_proj(act) (one GEMM over K = n_q d + I), plus
 //                the deepstack row add after the first layers
+//   EPI_RESID_LN EPI_RESID followed by the next layer's LayerNorm of the updated rows
+//                (units in row-block order; a half-full last round runs as tile halves)
 //   EPI_F32      alpha * acc (+ c): plain GEMM and the tied head's logit_scale footer.
 #include "kernels.h"
 #include "ptx.cuh"
